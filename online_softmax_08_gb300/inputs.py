@@ -1,0 +1,76 @@
+"""Seeded synthetic inputs and the workload table.
+
+This module draws random numbers and nothing else: it holds none of the
+attention arithmetic, so both the CUDA path and the fp64 oracle can be fed
+from it.  Every tensor is drawn in fp32 on the CPU from a ``torch.Generator``
+seeded with the workload's seed, in the fixed order Q, K, V, dO, and then
+rounded to bf16.  The oracle receives the same bf16 values upcast to fp64, so
+input quantisation is never counted as kernel error.
+
+Distributions follow the workloads: Q, K, V, dO ~ N(0, 1), except the
+logit-stress workload, where Q ~ 4 N(0, 1) (scores with standard deviation 4,
+so the running maximum keeps rising late in a row) and V ~ U(-1, 1).
+"""
+import math
+
+import torch
+
+# name -> shape, causal modes, passes, distribution knobs, seed.
+# "slice" marks the reduced case on which the long-sequence backward is checked.
+WORKLOADS = {
+    "single_head_n256_d64": dict(B=1, H=1, N=256, d=64, causal=(False,), passes=("fwd",),
+                                 q_std=1.0, v_dist="normal", seed=1235),
+    "b4h16_n2048_d64": dict(B=4, H=16, N=2048, d=64, causal=(False, True), passes=("fwd", "bwd"),
+                            q_std=1.0, v_dist="normal", seed=1236),
+    "b1h32_n8192_d128_causal": dict(B=1, H=32, N=8192, d=128, causal=(True,), passes=("fwd", "bwd"),
+                                    q_std=1.0, v_dist="normal", seed=1237),
+    "logit_stress_b2h16_n4000_d128": dict(B=2, H=16, N=4000, d=128, causal=(False,), passes=("fwd",),
+                                          q_std=4.0, v_dist="uniform", seed=1238),
+    "long_b1h16_n32768_d128_causal": dict(B=1, H=16, N=32768, d=128, causal=(True,),
+                                          passes=("fwd", "bwd"), q_std=1.0, v_dist="normal", seed=1239),
+    "long_bwd_slice_b1h1_n4096_d128_causal": dict(B=1, H=1, N=4096, d=128, causal=(True,),
+                                                  passes=("bwd",), q_std=1.0, v_dist="normal",
+                                                  seed=1240),
+}
+
+HEADLINE = "b1h32_n8192_d128_causal"
+
+
+def default_scale(d):
+    """1/sqrt(d), the scale every workload uses."""
+    return 1.0 / math.sqrt(d)
+
+
+def make_inputs(B, H, N, d, seed, q_std=1.0, v_dist="normal", with_do=False):
+    """Return bf16 CPU tensors (q, k, v[, do]) of shape [B, H, N, d]."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    shape = (B, H, N, d)
+    q = torch.randn(shape, generator=g, dtype=torch.float32) * float(q_std)
+    k = torch.randn(shape, generator=g, dtype=torch.float32)
+    if v_dist == "normal":
+        v = torch.randn(shape, generator=g, dtype=torch.float32)
+    elif v_dist == "uniform":
+        v = torch.rand(shape, generator=g, dtype=torch.float32) * 2.0 - 1.0
+    else:
+        raise ValueError(v_dist)
+    out = [q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)]
+    if with_do:
+        out.append(torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16))
+    return tuple(out)
+
+
+def workload_inputs(name, with_do=False, **override):
+    """Inputs for a named workload; ``override`` may replace B, H, N, d or seed."""
+    w = dict(WORKLOADS[name])
+    w.update(override)
+    return make_inputs(w["B"], w["H"], w["N"], w["d"], w["seed"], w["q_std"], w["v_dist"], with_do)
+
+
+def sample_rows(N, count, seed, always=(0, 127, 128)):
+    """Seeded query-row sample: the listed rows, N-1, then uniform draws."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    rows = [r for r in always if r < N] + [N - 1]
+    extra = torch.randint(0, N, (max(0, count - len(rows)),), generator=g).tolist()
+    return sorted(set(rows + extra))

@@ -1,0 +1,145 @@
+"""fp64 CPU oracle for scaled dot-product attention.  TEST INFRASTRUCTURE ONLY.
+
+Only tests/, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` leg of
+``bench.py`` may import this package.  It is independent of the CUDA path:
+the two share no code, and nothing here imports ``online_softmax_08_gb300``.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, OpenMP loops); this module
+compiles it on demand with gcc and marshals numpy arrays through ctypes.
+
+  attention_fwd       -- S = scale Q K^T, three-pass safe softmax, O = P V, LSE
+  attention_fwd_rows  -- the same definition for sampled (head, query row) pairs
+  attention_bwd       -- the textbook backward (dQ, dK, dV) of that definition
+  tile_counts         -- brute-force full / masked / skipped tile classification
+
+Inputs are numpy float64 arrays of shape [B, H, N, d] (contiguous).
+"""
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force=False):
+    """Compile oracle.c into liboracle.so (gcc, -O2, OpenMP, no FMA contraction)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-Wall", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        dp = ctypes.POINTER(ctypes.c_double)
+        lp = ctypes.POINTER(ctypes.c_int64)
+        i64, c_int, c_double = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, i64, i64, i64, c_double, c_int, c_int]
+        lib.oracle_attn_fwd_rows.argtypes = [dp, dp, dp, i64, i64, i64, c_double, c_int, lp, lp,
+                                             i64, dp, dp, c_int]
+        lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, i64, i64, i64, c_double, c_int, lp, i64,
+                                        dp, dp, dp, c_int]
+        lib.oracle_tile_counts.argtypes = [i64, c_int, i64, i64, lp]
+        lib.oracle_max_threads.argtypes = []
+        for f in (lib.oracle_attn_fwd, lib.oracle_attn_fwd_rows, lib.oracle_attn_bwd,
+                  lib.oracle_tile_counts, lib.oracle_max_threads):
+            f.restype = c_int
+        _lib = lib
+        return lib
+
+
+def _f64(a):
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _i64(a):
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.int64))
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise RuntimeError("oracle %s failed with code %d" % (what, rc))
+
+
+def max_threads():
+    return _load().oracle_max_threads()
+
+
+def attention_fwd(q, k, v, scale, causal, nthreads=0):
+    """O [B,H,N,d] and LSE [B,H,N] (natural log) of softmax(scale Q K^T) V."""
+    lib = _load()
+    B, H, N, d = q.shape
+    q, qp = _f64(q)
+    k, kp = _f64(k)
+    v, vp = _f64(v)
+    o, op = _f64(np.empty((B, H, N, d)))
+    lse, lp_ = _f64(np.empty((B, H, N)))
+    _check(lib.oracle_attn_fwd(qp, kp, vp, op, lp_, B * H, N, d, float(scale), int(bool(causal)),
+                               int(nthreads)), "fwd")
+    return o, lse
+
+
+def attention_fwd_rows(q, k, v, scale, causal, bh_idx, row_idx, nthreads=0):
+    """Output rows o [count, d] and lse [count] for the sampled (b*H+h, row) pairs."""
+    lib = _load()
+    B, H, N, d = q.shape
+    q, qp = _f64(q)
+    k, kp = _f64(k)
+    v, vp = _f64(v)
+    bh, bhp = _i64(bh_idx)
+    rows, rp = _i64(row_idx)
+    if bh.shape != rows.shape:
+        raise ValueError("bh_idx and row_idx differ in length")
+    o, op = _f64(np.empty((len(rows), d)))
+    lse, lp_ = _f64(np.empty((len(rows),)))
+    _check(lib.oracle_attn_fwd_rows(qp, kp, vp, B * H, N, d, float(scale), int(bool(causal)), bhp,
+                                    rp, len(rows), op, lp_, int(nthreads)), "fwd_rows")
+    return o, lse
+
+
+def attention_bwd(q, k, v, do, scale, causal, heads=None, nthreads=0):
+    """dQ, dK, dV of sum(O * dO).  With ``heads`` (flat b*H+h indices) only those
+    heads are computed and the outputs are [len(heads), N, d]; otherwise
+    [B, H, N, d]."""
+    lib = _load()
+    B, H, N, d = q.shape
+    q, qp = _f64(q)
+    k, kp = _f64(k)
+    v, vp = _f64(v)
+    do, dop = _f64(do)
+    if heads is None:
+        nh, hp, shape = B * H, None, (B, H, N, d)
+    else:
+        hs, hp = _i64(heads)
+        nh, shape = len(hs), (len(hs), N, d)
+    dq, dqp = _f64(np.empty(shape))
+    dk, dkp = _f64(np.empty(shape))
+    dv, dvp = _f64(np.empty(shape))
+    _check(lib.oracle_attn_bwd(qp, kp, vp, dop, B * H, N, d, float(scale), int(bool(causal)), hp, nh,
+                               dqp, dkp, dvp, int(nthreads)), "bwd")
+    return dq, dk, dv
+
+
+def tile_counts(N, causal, block_q, block_k):
+    """(full, masked, skipped) tiles of one head's grid."""
+    lib = _load()
+    out, op = _i64(np.zeros(3))
+    _check(lib.oracle_tile_counts(int(N), int(bool(causal)), int(block_q), int(block_k), op), "tiles")
+    return tuple(int(x) for x in out)

@@ -1,0 +1,114 @@
+/*
+ * fattn.h -- C-ABI of libfattn: exact tiled scaled-dot-product attention
+ * (FlashAttention forward and backward) for NVIDIA GB300 (sm_103a).
+ *
+ * The operation, for every (batch b, head h) independently
+ * ("FlashAttention tiles exact softmax without materializing the score
+ * matrix", opening equations; "tm_flash_attention_math", "What we must
+ * compute, and why storage is the problem"):
+ *
+ *     S = scale * Q K^T            (N x N, never stored)
+ *     P = softmax(S) row by row    (causal: key j visible to query i iff j <= i)
+ *     O = P V
+ *     LSE_i = m_i + ln l_i = ln sum_j exp(S_ij)
+ *
+ * LSE is the one per-row statistic the backward pass keeps ("Decoding flash
+ * attention", "The backward pass"); the backward recomputes P = exp(S - LSE)
+ * tile by tile and returns dQ, dK, dV of a loss whose gradient w.r.t. O is dO.
+ *
+ * Layout.  q, k, v, o, dout, dq, dk, dv are DEVICE pointers to contiguous
+ * bf16 tensors [B, H, N, d] (row-major, d innermost).  lse is a DEVICE
+ * pointer to fp32 [B, H, N].  Every pointer must be 16-byte aligned.
+ * d must be 64 or 128.  N >= 1, B >= 1, H >= 1, B*H*N < 2^31.
+ * scale must be finite and > 0 (every workload here uses 1/sqrt(d)).
+ *
+ * Ownership.  The caller allocates and owns every buffer; the library keeps
+ * no per-call state and never frees caller memory.
+ *
+ * Streams and errors.  Calls are asynchronous on `stream` (a cudaStream_t;
+ * NULL is the legacy default stream).  Arguments are validated before
+ * anything is launched: a bad argument returns a non-zero status and
+ * launches nothing.  A launch failure returns FATTN_ERR_CUDA.  Faults during
+ * execution surface at the caller's next synchronisation, as usual in CUDA.
+ * Every wait inside a kernel is bounded; a wait that runs out records a code
+ * in a device error word (read with fattn_device_error) and the kernel
+ * finishes without hanging.
+ *
+ * The device must be compute capability 10.3 (sm_103a), else
+ * FATTN_ERR_UNSUPPORTED.
+ */
+#ifndef FATTN_H_
+#define FATTN_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FATTN_OK = 0,
+  FATTN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, bad scale */
+  FATTN_ERR_UNSUPPORTED = 2, /* d not in {64,128}, or the device is not sm_103 */
+  FATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a launch failed */
+  FATTN_ERR_WORKSPACE = 4,   /* workspace missing or too small */
+  FATTN_ERR_TIMEOUT = 5      /* a bounded in-kernel wait ran out (fattn_device_error) */
+} fattn_status;
+
+/* Forward pass.  Writes o [B,H,N,d] bf16 and lse [B,H,N] fp32 (natural log,
+ * in units of scaled scores).  The online-softmax state (running max m,
+ * running sum l, unnormalised accumulator o~, rescale alpha = exp(m_old - m_new))
+ * is carried across 128-key tiles ("tm_flash_attention_math", "The block-wise
+ * update, and the full algorithm"); key tiles wholly above the causal
+ * diagonal are skipped and only diagonal-crossing or ragged tiles are masked
+ * element by element (page 1, "Causal masking fits inside the tiled
+ * computation"). */
+int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int N, int d, float scale, int causal, void* stream);
+
+/* fattn_fwd plus tile instrumentation: when tile_counts (DEVICE pointer to 3
+ * unsigned 64-bit counters) is not NULL, the kernel ADDS the number of
+ * (128-row query tile, 128-key tile) pairs it processed without masks
+ * [0], processed with element masks [1], and skipped as wholly above the
+ * causal diagonal [2].  The caller zeroes the counters. */
+int fattn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, unsigned long long* tile_counts,
+                 void* stream);
+
+/* Bytes of device workspace fattn_bwd needs: an fp32 dQ accumulator
+ * [B,H,N,d] and the fp32 row statistic D [B,H,N]. */
+size_t fattn_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/* Backward pass.  Inputs q, k, v, o, lse as produced by fattn_fwd and dout
+ * = dL/dO; outputs dq, dk, dv [B,H,N,d] bf16.  The pages give no gradient
+ * formulas; the calculus of the definition is used: D_i = sum_c dO_ic O_ic,
+ * P = exp(S - LSE), dV = P^T dO, dP = dO V^T, dS = P o (dP - D),
+ * dQ = scale dS K, dK = scale dS^T Q ("FlashAttention tiles exact softmax
+ * without materializing the score matrix", "Backward computation can trade
+ * recomputation for stored intermediates").
+ * workspace: DEVICE memory of at least fattn_bwd_workspace_bytes(B,H,N,d)
+ * bytes, 256-byte aligned, owned by the caller; its contents on entry do not
+ * matter and are overwritten.  NULL or too small -> FATTN_ERR_WORKSPACE. */
+int fattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+              const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+              float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Tile shape used by a pass (0 = forward, 1 = backward) for head size d:
+ * rows of Q per tile and keys per K/V tile.  Returns FATTN_OK or
+ * FATTN_ERR_UNSUPPORTED. */
+int fattn_tile_sizes(int d, int pass, int* block_q, int* block_k);
+
+/* Read (and, if clear != 0, reset) the device error word of the current
+ * device: 0 if no in-kernel wait ran out since the last reset, else the code
+ * of the first one.  Synchronises the device.  Returns FATTN_OK or
+ * FATTN_ERR_CUDA. */
+int fattn_device_error(unsigned int* code, int clear);
+
+/* Human-readable name of a status code (static storage). */
+const char* fattn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FATTN_H_ */

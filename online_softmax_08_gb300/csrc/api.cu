@@ -1,0 +1,222 @@
+// api.cu -- the C-ABI of libfattn: argument checks, TMA descriptors, launches.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "../../include/fattn.h"
+#include "common.cuh"
+
+namespace fattn {
+namespace {
+
+__device__ unsigned int g_error_word;  // first in-kernel wait that ran out (0 = none)
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool probed = false;
+  bool supported = false;
+  unsigned int* err = nullptr;  // device address of g_error_word
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& info = g_dev[dev];
+  if (!info.probed) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FATTN_ERR_CUDA;
+    info.supported = (major == 10 && minor == 3);
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_error_word) != cudaSuccess) return FATTN_ERR_CUDA;
+    info.err = static_cast<unsigned int*>(addr);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return FATTN_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    info.probed = true;
+  }
+  if (!info.supported) return FATTN_ERR_UNSUPPORTED;
+  *out = &info;
+  return FATTN_OK;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D map over a [BH, N, inner] tensor (inner contiguous), box {box0, box1, 1}.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes,
+              long long inner, long long N, long long BH, int box0, int box1,
+              CUtensorMapSwizzle swz) {
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)(inner * elem_bytes), (cuuint64_t)(inner * N * elem_bytes)};
+  cuuint32_t box[3] = {(cuuint32_t)box0, (cuuint32_t)box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool make_bf16_map(CUtensorMap* m, const void* base, int d, long long N, long long BH, int rows) {
+  return make_map(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64, rows,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+int check_common(int B, int H, int N, int d, float scale) {
+  if (B < 1 || H < 1 || N < 1) return FATTN_ERR_INVALID_ARG;
+  if ((long long)B * H * N >= (1LL << 31)) return FATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  return FATTN_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+}  // namespace fattn
+
+using namespace fattn;
+
+extern "C" int fattn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int H, int N, int d, float scale, int causal,
+                            unsigned long long* tile_counts, void* stream) {
+  int st = check_common(B, H, N, d, scale);
+  if (st != FATTN_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FATTN_ERR_INVALID_ARG;
+  if (tile_counts && (reinterpret_cast<uintptr_t>(tile_counts) & 7u)) return FATTN_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  st = current_device(&dev);
+  if (st != FATTN_OK) return st;
+  const long long BH = (long long)B * H;
+  CUtensorMap tq, tk, tv, to;
+  if (!make_bf16_map(&tq, q, d, N, BH, 128) || !make_bf16_map(&tk, k, d, N, BH, 128) ||
+      !make_bf16_map(&tv, v, d, N, BH, 128) || !make_bf16_map(&to, o, d, N, BH, 128))
+    return FATTN_ERR_CUDA;
+  FwdParams p;
+  p.BH = (int)BH;
+  p.N = N;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.lse = lse;
+  p.tiles = tile_counts;
+  p.err = dev->err;
+  cudaError_t e = launch_fwd(d, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
+extern "C" int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int d, float scale, int causal, void* stream) {
+  return fattn_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, nullptr, stream);
+}
+
+extern "C" size_t fattn_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  const size_t rows = (size_t)B * H * N;
+  return align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+extern "C" int fattn_bwd(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, float scale, int causal, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  int st = check_common(B, H, N, d, scale);
+  if (st != FATTN_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FATTN_ERR_INVALID_ARG;
+  const size_t need = fattn_bwd_workspace_bytes(B, H, N, d);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return FATTN_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  st = current_device(&dev);
+  if (st != FATTN_OK) return st;
+  const long long BH = (long long)B * H;
+  const long long rows = BH * N;
+  float* dq_acc = static_cast<float*>(workspace);
+  float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          align256((size_t)rows * d * sizeof(float)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int bq = 0, bk = 0;
+  fattn_tile_sizes(d, 1, &bq, &bk);
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
+  if (!make_bf16_map(&tq, q, d, N, BH, bq) || !make_bf16_map(&tdo, dout, d, N, BH, bq) ||
+      !make_bf16_map(&tk, k, d, N, BH, bk) || !make_bf16_map(&tv, v, d, N, BH, bk) ||
+      !make_bf16_map(&tdk, dk, d, N, BH, bk) || !make_bf16_map(&tdv, dv, d, N, BH, bk))
+    return FATTN_ERR_CUDA;
+  // dQ accumulator: fp32, add-reduced tile by tile
+  const bool ok = (d == 128)
+                      ? make_map(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, BH, 128,
+                                 bq, CU_TENSOR_MAP_SWIZZLE_NONE)
+                      : make_map(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, BH, 32,
+                                 bq, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return FATTN_ERR_CUDA;
+  if (launch_bwd_preprocess(o, dout, delta, dq_acc, rows, d, s) != cudaSuccess)
+    return FATTN_ERR_CUDA;
+  BwdParams p;
+  p.BH = (int)BH;
+  p.N = N;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.lse = lse;
+  p.delta = delta;
+  p.err = dev->err;
+  cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, tdk, tdv, tdq, p, s);
+  if (e == cudaErrorNotSupported) return FATTN_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return FATTN_ERR_CUDA;
+  if (launch_bwd_convert(dq_acc, dq, rows * d, scale, s) != cudaSuccess) return FATTN_ERR_CUDA;
+  return FATTN_OK;
+}
+
+extern "C" int fattn_tile_sizes(int d, int pass, int* block_q, int* block_k) {
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  if (pass != 0 && pass != 1) return FATTN_ERR_INVALID_ARG;
+  int bq = 128, bk = 128;
+  if (pass == 1) bq = (d == 128) ? 64 : 128;
+  if (block_q) *block_q = bq;
+  if (block_k) *block_k = bk;
+  return FATTN_OK;
+}
+
+extern "C" int fattn_device_error(unsigned int* code, int clear) {
+  if (!code) return FATTN_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FATTN_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v)) != cudaSuccess) return FATTN_ERR_CUDA;
+  *code = v;
+  if (clear && v) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess)
+      return FATTN_ERR_CUDA;
+  }
+  return FATTN_OK;
+}
+
+extern "C" const char* fattn_status_string(int status) {
+  switch (status) {
+    case FATTN_OK: return "ok";
+    case FATTN_ERR_INVALID_ARG: return "invalid argument";
+    case FATTN_ERR_UNSUPPORTED: return "unsupported head size or device";
+    case FATTN_ERR_CUDA: return "CUDA error";
+    case FATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case FATTN_ERR_TIMEOUT: return "in-kernel wait timed out";
+    default: return "unknown status";
+  }
+}

@@ -1,0 +1,401 @@
+// fwd.cu -- FlashAttention forward for sm_103a (tcgen05 + TMEM + TMA).
+//
+// One CTA owns 256 query rows of one (batch, head): two 128-row subtiles
+// Q_0, Q_1 ("In a real kernel this loop runs for a whole tile of queries at
+// once", tm_flash_attention_math, "The block-wise update, and the full
+// algorithm").  K/V tiles of 128 keys stream through a ring of shared-memory
+// slots filled by TMA; the score tile S = Q K^T lives only in TMEM
+// ("A score tile is temporary state", page "FlashAttention tiles exact
+// softmax without materializing the score matrix").
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax for Q_0, warps 4-7 softmax for Q_1: thread t owns query
+//              row t, which is TMEM lane t, so the row max and row sum need no
+//              shuffles.  They also rescale their O accumulator by alpha and
+//              run the epilogue O = o~ / l, LSE = m + ln l.
+//   warp 8     one thread issues every tcgen05.mma and commit.
+//   warp 9     one thread issues every TMA load.
+//
+// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 after it.
+// Shared memory: Q_0, Q_1 | K/V ring | P_0, P_1 (bf16, 128B-swizzled K-major).
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace fattn {
+namespace {
+
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct Fwd {
+  static constexpr int BM = 128;                  // rows per Q subtile
+  static constexpr int BN = 128;                  // keys per K/V tile
+  static constexpr int HALF = BM * 128;           // one 64-column, 128-row swizzled half (bytes)
+  static constexpr int TILE = BM * D * 2;         // Q, K, V or O tile (bf16)
+  static constexpr int PTILE = BM * BN * 2;       // P tile (bf16)
+  static constexpr int STAGES = D == 128 ? 3 : 6; // K/V ring slots
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + 2 * TILE;
+  static constexpr int OFF_P = OFF_KV + STAGES * TILE;
+  static constexpr int OFF_BAR = OFF_P + 2 * PTILE;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers + alignment slack
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t TM_S = 0;
+  static constexpr uint32_t TM_O = 256;
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, false, false);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
+};
+
+// Barrier slots (8 bytes each) inside the OFF_BAR block.
+enum {
+  B_Q = 0,
+  B_S_FULL = 1,   // [2] MMA -> softmax: S_s ready in TMEM
+  B_S_FREE = 3,   // [2] softmax -> MMA: S_s copied to registers
+  B_P_FULL = 5,   // [2] softmax -> MMA: P_s in smem and O_s rescaled
+  B_PV_DONE = 7,  // [2] MMA -> softmax: O_s += P_s V finished
+  B_MMA_DONE = 9,
+  B_KV_FULL = 10,  // [STAGES]
+};
+
+template <int D>
+__global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
+    fattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
+  using C = Fwd<D>;
+  constexpr int ST = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = p.N;
+  const int n_qb = (N + 255) / 256;
+  // heaviest (last) query blocks first
+  const int qb = n_qb - 1 - (int)(blockIdx.x / (unsigned)p.BH);
+  const int bh = (int)(blockIdx.x % (unsigned)p.BH);
+  const int n_kv_total = (N + C::BN - 1) / C::BN;
+
+  // rows [r0_s, r0_s + 128) of subtile s see key tiles [0, nt_s)
+  auto tiles_for = [&](int r0) {
+    if (r0 >= N) return 0;
+    const int last_key = p.causal ? min(r0 + C::BM - 1, N - 1) : N - 1;
+    return last_key / C::BN + 1;
+  };
+  const int r0_0 = qb * 256, r0_1 = qb * 256 + 128;
+  const int nt0 = tiles_for(r0_0), nt1 = tiles_for(r0_1);
+  const int r0[2] = {r0_0, r0_1};
+  const int nt[2] = {nt0, nt1};
+  const int n_max = max(nt0, nt1);
+
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  const uint32_t kv_full0 = bar(B_KV_FULL), kv_empty0 = bar(B_KV_FULL + ST);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * (B_KV_FULL + 2 * ST));
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  const WaitCtx wctx{abort_flag, p.err};
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_Q), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_S_FULL + s), 1);
+      mbar_init(bar(B_S_FREE + s), 128);
+      mbar_init(bar(B_P_FULL + s), 128);
+      mbar_init(bar(B_PV_DONE + s), 1);
+    }
+    mbar_init(bar(B_MMA_DONE), 1);
+    for (int i = 0; i < ST; ++i) {
+      mbar_init(kv_full0 + 8u * i, 1);
+      mbar_init(kv_empty0 + 8u * i, 1);
+    }
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 9) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const uint32_t q_bytes = (uint32_t)((nt0 > 0) + (nt1 > 0)) * C::TILE;
+      mbar_arrive_expect_tx(bar(B_Q), q_bytes);
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+        if (nt[s] > 0)
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(sbase + C::OFF_Q + s * C::TILE + h * C::HALF, &tm_q, bar(B_Q), h * 64,
+                        r0[s], bh);
+      const int n_loads = 2 * n_max;
+      for (int i = 0; i < n_loads; ++i) {
+        const int slot = i % ST, use = i / ST;
+        if (use > 0) mbar_wait(kv_empty0 + 8u * slot, (use - 1) & 1, wctx, ERR_SITE_FWD | 0x01);
+        const uint32_t dst = sbase + C::OFF_KV + slot * C::TILE;
+        const CUtensorMap* m = (i & 1) ? &tm_v : &tm_k;
+        mbar_arrive_expect_tx(kv_full0 + 8u * slot, C::TILE);
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(dst + h * C::HALF, m, kv_full0 + 8u * slot, h * 64, (i >> 1) * C::BN, bh);
+      }
+      // make sure no load is still landing when the CTA leaves
+      for (int i = max(0, n_loads - ST); i < n_loads; ++i)
+        mbar_wait(kv_full0 + 8u * (i % ST), (i / ST) & 1, wctx, ERR_SITE_FWD | 0x02);
+      mbar_wait(bar(B_Q), 0, wctx, ERR_SITE_FWD | 0x03);
+    }
+    __syncwarp();
+  } else if (warp == 8) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      auto kv_wait = [&](int i) {
+        mbar_wait(kv_full0 + 8u * (i % ST), (i / ST) & 1, wctx, ERR_SITE_FWD | 0x11);
+      };
+      auto issue_s = [&](int s, int j) {  // S_s = Q_s K_j^T
+        const uint32_t a = sbase + C::OFF_Q + s * C::TILE;
+        const uint32_t b = sbase + C::OFF_KV + ((2 * j) % ST) * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::HALF + (kk & 3) * 32;
+          mma_bf16_ss(tmem + C::TM_S + s * 128, sdesc_sw128(a + off, 16, 1024),
+                      sdesc_sw128(b + off, 16, 1024), C::IDESC_S, kk > 0);
+        }
+        mma_commit(bar(B_S_FULL + s));
+      };
+      auto issue_pv = [&](int s, int j) {  // O_s += P_s V_j
+        const uint32_t a = sbase + C::OFF_P + s * C::PTILE;
+        const uint32_t b = sbase + C::OFF_KV + ((2 * j + 1) % ST) * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk) {
+          const uint32_t a_off = (kk >> 2) * C::HALF + (kk & 3) * 32;
+          const uint32_t b_off = kk * 16 * 128;
+          mma_bf16_ss(tmem + C::TM_O + s * D, sdesc_sw128(a + a_off, 16, 1024),
+                      sdesc_sw128(b + b_off, C::HALF, 1024), C::IDESC_PV, (j > 0 || kk > 0));
+        }
+        mma_commit(bar(B_PV_DONE + s));
+      };
+      mbar_wait(bar(B_Q), 0, wctx, ERR_SITE_FWD | 0x12);
+      if (n_max > 0) {
+        kv_wait(0);
+        tc_fence_after();
+        if (nt0 > 0) issue_s(0, 0);
+        if (nt1 > 0) issue_s(1, 0);
+        mma_commit(kv_empty0 + 8u * 0);
+      }
+      for (int j = 0; j < n_max; ++j) {
+        const bool next = j + 1 < n_max;
+        if (next) kv_wait(2 * (j + 1));
+        if (j + 1 < nt0) {
+          mbar_wait(bar(B_S_FREE + 0), j & 1, wctx, ERR_SITE_FWD | 0x13);
+          tc_fence_after();
+          issue_s(0, j + 1);
+        }
+        if (j < nt0) {
+          kv_wait(2 * j + 1);
+          mbar_wait(bar(B_P_FULL + 0), j & 1, wctx, ERR_SITE_FWD | 0x14);
+          tc_fence_after();
+          issue_pv(0, j);
+        }
+        if (j + 1 < nt1) {
+          mbar_wait(bar(B_S_FREE + 1), j & 1, wctx, ERR_SITE_FWD | 0x15);
+          tc_fence_after();
+          issue_s(1, j + 1);
+        }
+        if (next) mma_commit(kv_empty0 + 8u * ((2 * (j + 1)) % ST));
+        if (j < nt1) {
+          kv_wait(2 * j + 1);
+          mbar_wait(bar(B_P_FULL + 1), j & 1, wctx, ERR_SITE_FWD | 0x16);
+          tc_fence_after();
+          issue_pv(1, j);
+        }
+        mma_commit(kv_empty0 + 8u * ((2 * j + 1) % ST));
+      }
+      mma_commit(bar(B_MMA_DONE));
+      mbar_wait(bar(B_MMA_DONE), 0, wctx, ERR_SITE_FWD | 0x17);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- softmax (warps 0-7)
+    const int s = warp >> 2;
+    const int t = threadIdx.x & 127;  // row in the subtile == TMEM lane
+    const int my_r0 = s ? r0_1 : r0_0;
+    const int my_nt = s ? nt1 : nt0;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::TM_S + s * 128;
+    const uint32_t tO = tmem + lane_off + C::TM_O + s * D;
+    const int row = my_r0 + t;
+    const float sl2 = p.scale_log2;
+    const uint32_t p_base = sbase + C::OFF_P + s * C::PTILE;
+    float m_run = -INFINITY, l_run = 0.f;
+    unsigned long long n_full = 0, n_masked = 0;
+
+    for (int j = 0; j < my_nt; ++j) {
+      mbar_wait(bar(B_S_FULL + s), j & 1, wctx, ERR_SITE_FWD | 0x21);
+      tc_fence_after();
+      uint32_t u[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, u[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_fence32(u[c]);
+      tc_fence_before();
+      mbar_arrive(bar(B_S_FREE + s));
+
+      float sv[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(u[c][i]);
+
+      // masks go in before the block maximum
+      const int c0 = j * C::BN;
+      const bool need_mask =
+          (p.causal && min(c0 + C::BN - 1, N - 1) > my_r0) || (c0 + C::BN > N);
+      if (need_mask) {
+        int lim = N - c0;
+        if (p.causal) lim = min(lim, row - c0 + 1);
+#pragma unroll
+        for (int k = 0; k < 128; ++k)
+          if (k >= lim) sv[k] = -INFINITY;
+        ++n_masked;
+      } else {
+        ++n_full;
+      }
+
+      float mx0 = m_run, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 128; k += 4) {
+        mx0 = fmaxf(mx0, sv[k]);
+        mx1 = fmaxf(mx1, sv[k + 1]);
+        mx2 = fmaxf(mx2, sv[k + 2]);
+        mx3 = fmaxf(mx3, sv[k + 3]);
+      }
+      const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      const float msc = (m_new == -INFINITY) ? 0.f : m_new * sl2;
+      const float alpha = ex2(m_run * sl2 - msc);  // exp(m_old - m_new); 0 on the first block
+      const bool rescale = m_new != m_run;
+      float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
+#pragma unroll
+      for (int k = 0; k < 128; k += 4) {
+        sv[k] = ex2(fmaf(sv[k], sl2, -msc));
+        sv[k + 1] = ex2(fmaf(sv[k + 1], sl2, -msc));
+        sv[k + 2] = ex2(fmaf(sv[k + 2], sl2, -msc));
+        sv[k + 3] = ex2(fmaf(sv[k + 3], sl2, -msc));
+        ls0 += sv[k];
+        ls1 += sv[k + 1];
+        ls2 += sv[k + 2];
+        ls3 += sv[k + 3];
+      }
+      l_run = l_run * alpha + ((ls0 + ls1) + (ls2 + ls3));
+      m_run = m_new;
+
+      // P_s and O_s are still in use by the previous O_s += P_s V
+      if (j > 0) {
+        mbar_wait(bar(B_PV_DONE + s), (j - 1) & 1, wctx, ERR_SITE_FWD | 0x22);
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {  // 16 chunks of 8 keys; two 64-key swizzled halves
+        const uint32_t addr = p_base + (c >> 3) * C::HALF + t * 128 + (((c & 7) ^ (t & 7)) << 4);
+        st_shared_v4(addr, pack_bf16x2(sv[8 * c], sv[8 * c + 1]),
+                     pack_bf16x2(sv[8 * c + 2], sv[8 * c + 3]),
+                     pack_bf16x2(sv[8 * c + 4], sv[8 * c + 5]),
+                     pack_bf16x2(sv[8 * c + 6], sv[8 * c + 7]));
+      }
+      fence_proxy_async_smem();
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_wait_ld(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + c * 32, o);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(B_P_FULL + s));
+    }
+
+    if (my_nt > 0) {
+      // ------------------------------------------------------------ epilogue
+      mbar_wait(bar(B_PV_DONE + s), (my_nt - 1) & 1, wctx, ERR_SITE_FWD | 0x23);
+      tc_fence_after();
+      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+      const uint32_t o_base = sbase + C::OFF_Q + s * C::TILE;  // Q_s is no longer read
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_wait_ld(o);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {  // four 16-byte chunks of 8 columns
+          const int col = c * 32 + q4 * 8;
+          const int half = col >> 6, chunk = (col & 63) >> 3;
+          const uint32_t addr = o_base + half * C::HALF + t * 128 + ((chunk ^ (t & 7)) << 4);
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[q4 * 8 + e]) * inv_l;
+          st_shared_v4(addr, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                       pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1 + s, 128);
+      if (t == 0) {
+        for (int h = 0; h < D / 64; ++h) tma_store_3d(&tm_o, o_base + h * C::HALF, h * 64, my_r0, bh);
+        bulk_commit();
+        bulk_wait_all();
+      }
+      if (row < N) p.lse[(size_t)bh * N + row] = (m_run * sl2 + lg2(l_run)) * kLn2;
+      if (p.tiles && t == 0) {
+        atomicAdd(p.tiles + 0, n_full);
+        atomicAdd(p.tiles + 1, n_masked);
+        atomicAdd(p.tiles + 2, (unsigned long long)(p.causal ? n_kv_total - my_nt : 0));
+      }
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                   const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
+  using C = Fwd<D>;
+  static_assert(C::SMEM <= 232448, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(fattn_fwd_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const long long n_qb = (p.N + 255) / 256;
+  const long long blocks = n_qb * p.BH;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  fattn_fwd_kernel<D><<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, to, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
+  if (d == 128) return launch<128>(tq, tk, tv, to, p, stream);
+  if (d == 64) return launch<64>(tq, tk, tv, to, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fattn

@@ -1,0 +1,159 @@
+"""ctypes binding of libfattn (argument marshalling only).
+
+The functions named like the C entry points (``fattn_fwd``, ``fattn_bwd``, ...)
+take torch tensors (or raw integer device addresses) and pass their pointers,
+sizes and the current CUDA stream straight to the library; every step of the
+computation runs in the library's kernels.  ``forward`` and ``backward``
+allocate the outputs with torch and then call those entry points.
+
+The library is loaded on first use.  If ``libfattn.so`` is missing the
+binding raises: there is no fallback path.
+"""
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfattn.so")
+
+FATTN_OK = 0
+STATUS_NAMES = {0: "FATTN_OK", 1: "FATTN_ERR_INVALID_ARG", 2: "FATTN_ERR_UNSUPPORTED",
+                3: "FATTN_ERR_CUDA", 4: "FATTN_ERR_WORKSPACE", 5: "FATTN_ERR_TIMEOUT"}
+
+# Every exported symbol of include/fattn.h: name -> (restype, argtypes)
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "fattn_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
+    "fattn_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp]),
+    "fattn_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "fattn_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp,
+                       _sz, _vp]),
+    "fattn_tile_sizes": (_i, [_i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
+    "fattn_device_error": (_i, [ctypes.POINTER(ctypes.c_uint), _i]),
+    "fattn_status_string": (ctypes.c_char_p, [_i]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FattnError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s returned %s (%d)" % (fn, STATUS_NAMES.get(status, "?"), status))
+
+
+def load(path=None):
+    """Load libfattn.so (once) and declare the C signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError("libfattn.so not found at %s: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`" % p)
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(name, status):
+    if status != FATTN_OK:
+        raise FattnError(name, status)
+
+
+# ------------------------------------------------------------------ entry points
+
+def fattn_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream=None):
+    _check("fattn_fwd", load().fattn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                         float(scale), int(bool(causal)), _stream(stream)))
+
+
+def fattn_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, tile_counts, stream=None):
+    _check("fattn_fwd_ex", load().fattn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
+                                               N, d, float(scale), int(bool(causal)),
+                                               _ptr(tile_counts), _stream(stream)))
+
+
+def fattn_bwd_workspace_bytes(B, H, N, d):
+    return int(load().fattn_bwd_workspace_bytes(B, H, N, d))
+
+
+def fattn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+              workspace_bytes, stream=None):
+    _check("fattn_bwd", load().fattn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                         _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                                         int(bool(causal)), _ptr(workspace), int(workspace_bytes),
+                                         _stream(stream)))
+
+
+def fattn_tile_sizes(d, pass_):
+    bq, bk = ctypes.c_int(0), ctypes.c_int(0)
+    _check("fattn_tile_sizes", load().fattn_tile_sizes(d, pass_, ctypes.byref(bq), ctypes.byref(bk)))
+    return bq.value, bk.value
+
+
+def fattn_device_error(clear=True):
+    code = ctypes.c_uint(0)
+    _check("fattn_device_error", load().fattn_device_error(ctypes.byref(code), int(bool(clear))))
+    return code.value
+
+
+def fattn_status_string(status):
+    return load().fattn_status_string(int(status)).decode()
+
+
+# ------------------------------------------------------------------ allocating wrappers
+
+def _shape(q):
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    return tuple(q.shape)
+
+
+def forward(q, k, v, scale, causal, tile_counts=None, stream=None):
+    """O, LSE of bf16 [B,H,N,d] device tensors q, k, v (contiguous)."""
+    B, H, N, d = _shape(q)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if tile_counts is None:
+        fattn_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
+    else:
+        fattn_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, tile_counts, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, lse, do, scale, causal, workspace=None, stream=None):
+    """dQ, dK, dV for dL/dO = do."""
+    B, H, N, d = _shape(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = fattn_bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    fattn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+              workspace.numel() * workspace.element_size(), stream)
+    return dq, dk, dv

@@ -1,0 +1,72 @@
+"""The C-ABI library loads and exports every entry point include/fattn.h
+declares; argument checks that fail before any device work run on the CPU."""
+import os
+import re
+
+import pytest
+
+from online_softmax_08_gb300 import build as fbuild
+from online_softmax_08_gb300 import fattn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fbuild.build()
+    return fattn.load()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(fattn_\w+)\s*\(", src,
+                                    flags=re.M))
+    return names
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    declared = _declared()
+    assert {"fattn_fwd", "fattn_bwd", "fattn_bwd_workspace_bytes"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+        assert name in fattn.SIGNATURES, name
+
+
+def test_status_strings(lib):
+    assert fattn.fattn_status_string(0) == "ok"
+    assert "workspace" in fattn.fattn_status_string(4)
+
+
+def test_tile_sizes(lib):
+    assert fattn.fattn_tile_sizes(128, 0) == (128, 128)
+    assert fattn.fattn_tile_sizes(64, 0) == (128, 128)
+    assert fattn.fattn_tile_sizes(128, 1) == (64, 128)
+    assert fattn.fattn_tile_sizes(64, 1) == (128, 128)
+    with pytest.raises(fattn.FattnError):
+        fattn.fattn_tile_sizes(96, 0)
+
+
+def test_workspace_bytes(lib):
+    n = fattn.fattn_bwd_workspace_bytes(2, 3, 100, 64)
+    rows = 2 * 3 * 100
+    assert n >= rows * 64 * 4 + rows * 4 and n % 256 == 0
+    assert fattn.fattn_bwd_workspace_bytes(1, 1, 1, 96) == 0
+
+
+def test_argument_checks_before_any_device_call(lib):
+    # every call here fails validation, which happens before the library
+    # touches the CUDA runtime, so no GPU is needed
+    a = 1 << 20  # a 16-byte-aligned address that is never dereferenced
+    assert lib.fattn_fwd(None, a, a, a, a, 1, 1, 128, 128, 0.1, 0, None) == 1
+    assert lib.fattn_fwd(a + 8, a, a, a, a, 1, 1, 128, 128, 0.1, 0, None) == 1
+    assert lib.fattn_fwd(a, a, a, a, a, 1, 1, 128, 80, 0.1, 0, None) == 2
+    assert lib.fattn_fwd(a, a, a, a, a, 0, 1, 128, 128, 0.1, 0, None) == 1
+    assert lib.fattn_fwd(a, a, a, a, a, 1, 1, 128, 128, 0.0, 0, None) == 1
+    assert lib.fattn_fwd(a, a, a, a, a, 1 << 16, 1 << 16, 1, 64, 0.1, 0, None) == 1
+    assert lib.fattn_bwd(a, a, a, a, a, a, a, a, a, 1, 1, 128, 128, 0.1, 1, None, 0, None) == 4
+    assert lib.fattn_bwd(a, a, a, a, a, a, a, a, a, 1, 1, 128, 128, 0.1, 1, a + 16, 1 << 30,
+                         None) == 4
+    assert lib.fattn_bwd(a, a, a, a, a, a, a, a, a, 1, 1, 128, 128, 0.1, 1, a, 16, None) == 4

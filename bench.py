@@ -1,0 +1,391 @@
+"""Benchmark: exact attention forward + backward on one GB300, B=1 H=32 N=8192 d=128 causal.
+
+One step = one pass of the whole hot path on one batch of synthetic bf16
+input already resident in HBM: fattn_fwd (O, LSE) then fattn_bwd (D
+preprocess, dK/dV/dQ main kernel, dQ convert).  FLOPs follow the workload's
+convention: forward 4*B*H*N^2*d, backward 2.5x that, both halved for causal.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own copy of the workload on its
+own GPU (independent problems, no collective on the data path: weak scaling);
+the timed region is bracketed by a barrier and a synchronize on both sides and
+the slowest rank's time is used.
+
+--impl reference times the fp64 CPU oracle, as it stands, on the host cores
+(one step = forward + backward of a bounded sample of the workload: one head,
+the first PREFIX tokens of the causal sequence).
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from online_softmax_08_gb300.inputs import HEADLINE, WORKLOADS, default_scale, make_inputs  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s, N=8192 d=128 bf16 causal; % of GB300 BF16 peak"
+UNIT = "TFLOP/s"
+REF_PREFIX = 2048        # tokens of one head per reference-arm step
+CPU_BASELINE_SECONDS = 12.0
+
+
+def flops(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d * (0.5 if causal else 1.0)
+    return f, 2.5 * f
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ multi-rank plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x, world, device):
+    """Largest value of a float over all ranks (identity for one rank)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ reference arm / CPU baseline
+
+def oracle_step(q, k, v, do, scale, causal, prefix):
+    """fp64 oracle forward + backward on one head, the first ``prefix`` tokens."""
+    import oracle
+    sl = (slice(0, 1), slice(0, 1), slice(0, prefix))
+    f64 = lambda t: t[sl].to(torch.float64).numpy()
+    qh, kh, vh, doh = f64(q), f64(k), f64(v), f64(do)
+    oracle.attention_fwd(qh, kh, vh, scale, causal)
+    oracle.attention_bwd(qh, kh, vh, doh, scale, causal)
+    f, b = flops(1, 1, prefix, q.shape[-1], causal)
+    return f + b
+
+
+def cpu_baseline(inputs, scale, causal, min_seconds=CPU_BASELINE_SECONDS, prefix=REF_PREFIX):
+    import oracle
+    q, k, v, do = inputs
+    done, t0 = 0.0, time.perf_counter()
+    steps = 0
+    while True:
+        done += oracle_step(q, k, v, do, scale, causal, prefix)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    return {"value": done / el / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": "fp64 oracle forward+backward of head 0, first %d tokens of the causal "
+                      "sequence, repeated %d times (%.1f s)" % (prefix, steps, el)}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = WORKLOADS[HEADLINE]
+    d = w["d"]
+    q, k, v, do = make_inputs(1, 1, REF_PREFIX, d, w["seed"], w["q_std"], w["v_dist"], with_do=True)
+    scale = default_scale(d)
+    for _ in range(args.warmup):
+        oracle_step(q, k, v, do, scale, True, REF_PREFIX)
+    t0 = time.perf_counter()
+    total = 0.0
+    for _ in range(args.steps):
+        total += oracle_step(q, k, v, do, scale, True, REF_PREFIX)
+    el = time.perf_counter() - t0
+    import oracle
+    value = total / el / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": HEADLINE, "B": 1, "H": 1, "N": REF_PREFIX, "d": d, "causal": True,
+                   "sample": "one head, first %d tokens" % REF_PREFIX},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": "fp64 oracle forward+backward, one head, first %d tokens of "
+                                   "the causal sequence per step" % REF_PREFIX},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args):
+    from online_softmax_08_gb300 import fattn
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    fattn.load()
+
+    w = WORKLOADS[args.workload]
+    B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"][-1]
+    scale = default_scale(d)
+    f_fwd, f_bwd = flops(B, H, N, d, causal)
+    do_fwd, do_bwd = args.passes in ("both", "fwd"), args.passes in ("both", "bwd")
+    host = make_inputs(B, H, N, d, w["seed"] + 1000 * rank, w["q_std"], w["v_dist"], with_do=True)
+    q, k, v, do = (x.to(device) for x in host)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fattn.fattn_bwd_workspace_bytes(B, H, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    K = args.steps
+    fwd_ev = [(ev(), ev()) for _ in range(K)]
+    bwd_ev = [[ev() for _ in range(4)] for _ in range(K)]
+
+    if not do_fwd:  # the backward alone still needs a forward's O and LSE
+        fattn.fattn_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
+
+    def step(i=None):
+        if do_fwd:
+            if i is not None:
+                fwd_ev[i][0].record(stream)
+            fattn.fattn_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
+            if i is not None:
+                fwd_ev[i][1].record(stream)
+        if do_bwd:
+            if i is not None:
+                fattn.fattn_bwd_ex(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, ws,
+                                   ws_bytes, bwd_ev[i], stream)
+            else:
+                fattn.fattn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, ws,
+                                ws_bytes, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    for pair in fwd_ev:  # materialise event handles outside the timed region
+        pair[0].record(stream)
+        pair[1].record(stream)
+    for evs in bwd_ev:
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize(device)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    t0, t1 = ev(), ev()
+    t0.record(stream)
+    for i in range(K):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, device)
+    assert fattn.fattn_device_error() == 0, "an in-kernel wait timed out"
+
+    nan = float("nan")
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_ev) if do_fwd else nan
+    pre_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in bwd_ev) if do_bwd else nan
+    main_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in bwd_ev) if do_bwd else nan
+    conv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in bwd_ev) if do_bwd else nan
+    ms_per_step = elapsed_ms / K
+    step_flops = (f_fwd if do_fwd else 0.0) + (f_bwd if do_bwd else 0.0)
+    value = world * step_flops / (ms_per_step * 1e-3) / 1e12
+    peak_tf, peak_hbm, peak_src = peaks()
+
+    # the dominant kernel by time is the backward main kernel; its algorithmic
+    # work is the 2.5x-forward FLOP count of the workload
+    main_tf = f_bwd / (main_ms * 1e-3) / 1e12
+    fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
+    rows = B * H * N
+    fwd_bytes = 4 * rows * d * 2 + rows * 4
+    roof = {"kernel": "fattn_bwd_kernel<%d>" % d, "bound": "tensor", "achieved": main_tf,
+            "peak": peak_tf, "unit": "TFLOP/s", "frac": main_tf / peak_tf,
+            "peak_source": peak_src + " (bf16 burst)", "traffic": None}
+    roof_fwd = {"kernel": "fattn_fwd_kernel<%d>" % d, "bound": "tensor", "achieved": fwd_tf,
+                "peak": peak_tf, "unit": "TFLOP/s", "frac": fwd_tf / peak_tf,
+                "peak_source": peak_src + " (bf16 burst)", "traffic": None,
+                "algorithmic_bytes": fwd_bytes}
+
+    # end to end through the C-ABI with host buffers: pinned H2D of Q, K, V, dO,
+    # forward, backward, D2H of O, LSE, dQ, dK, dV
+    e2e = None
+    if not args.no_e2e and args.passes == "both":
+        pin = [x.pin_memory() for x in host]
+        outs_h = [torch.empty_like(o, device="cpu").pin_memory(),
+                  torch.empty_like(lse, device="cpu").pin_memory(),
+                  torch.empty_like(dq, device="cpu").pin_memory(),
+                  torch.empty_like(dk, device="cpu").pin_memory(),
+                  torch.empty_like(dv, device="cpu").pin_memory()]
+        h2d = sum(x.numel() * x.element_size() for x in pin)
+        d2h = sum(x.numel() * x.element_size() for x in outs_h)
+
+        def e2e_step():
+            for dst, src in zip((q, k, v, do), pin):
+                dst.copy_(src, non_blocking=True)
+            step()
+            for dst, src in zip(outs_h, (o, lse, dq, dk, dv)):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        barrier(world)
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(K):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(world)
+        e2e_ms = max_over_ranks(a.elapsed_time(b), world, device) / K
+        e2e = {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == HEADLINE:
+        cpu = cpu_baseline(host, scale, causal)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d,
+                       "causal": causal, "passes": args.passes,
+                       "per_rank": "one full workload per GPU",
+                       "l2": "inputs larger than L2 (Q, K, V, dO: %.0f MB each)"
+                             % (B * H * N * d * 2 / 1e6)},
+            "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peak_tf},
+            "bwd": {"ms": pre_ms + main_ms + conv_ms, "preprocess_ms": pre_ms,
+                    "main_ms": main_ms, "convert_ms": conv_ms,
+                    "tflops": f_bwd / ((pre_ms + main_ms + conv_ms) * 1e-3) / 1e12},
+            "roofline": roof, "roofline_fwd": roof_fwd,
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": (int(do_fwd) + 3 * int(do_bwd)) * K,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS),
+                    help="profiling only: the benchmark's workload is the default")
+    ap.add_argument("--pass", dest="passes", default="both", choices=["both", "fwd", "bwd"],
+                    help="profiling only: time one pass; a benchmark step is both")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -93,6 +93,15 @@ int fattn_bwd(const void* q, const void* k, const void* v, const void* o, const 
               const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
               float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
 
+/* fattn_bwd plus phase timing: when phase_events is not NULL it points to 4
+ * cudaEvent_t handles (created by the caller) that are recorded on `stream`
+ * before the preprocess kernel, before the main kernel, after the main
+ * kernel and after the dQ convert kernel. */
+int fattn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 float scale, int causal, void* workspace, size_t workspace_bytes,
+                 void* const* phase_events, void* stream);
+
 /* Tile shape used by a pass (0 = forward, 1 = backward) for head size d:
  * rows of Q per tile and keys per K/V tile.  Returns FATTN_OK or
  * FATTN_ERR_UNSUPPORTED. */

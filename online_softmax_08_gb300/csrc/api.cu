@@ -132,10 +132,10 @@ extern "C" size_t fattn_bwd_workspace_bytes(int B, int H, int N, int d) {
   return align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
 }
 
-extern "C" int fattn_bwd(const void* q, const void* k, const void* v, const void* o,
-                         const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
-                         int H, int N, int d, float scale, int causal, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+extern "C" int fattn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                            int B, int H, int N, int d, float scale, int causal, void* workspace,
+                            size_t workspace_bytes, void* const* phase_events, void* stream) {
   int st = check_common(B, H, N, d, scale);
   if (st != FATTN_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
@@ -167,8 +167,14 @@ extern "C" int fattn_bwd(const void* q, const void* k, const void* v, const void
                       : make_map(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, BH, 32,
                                  bq, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return FATTN_ERR_CUDA;
+  auto mark = [&](int i) {
+    return !phase_events ||
+           cudaEventRecord(static_cast<cudaEvent_t>(phase_events[i]), s) == cudaSuccess;
+  };
+  if (!mark(0)) return FATTN_ERR_CUDA;
   if (launch_bwd_preprocess(o, dout, delta, dq_acc, rows, d, s) != cudaSuccess)
     return FATTN_ERR_CUDA;
+  if (!mark(1)) return FATTN_ERR_CUDA;
   BwdParams p;
   p.BH = (int)BH;
   p.N = N;
@@ -181,8 +187,18 @@ extern "C" int fattn_bwd(const void* q, const void* k, const void* v, const void
   cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, tdk, tdv, tdq, p, s);
   if (e == cudaErrorNotSupported) return FATTN_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return FATTN_ERR_CUDA;
+  if (!mark(2)) return FATTN_ERR_CUDA;
   if (launch_bwd_convert(dq_acc, dq, rows * d, scale, s) != cudaSuccess) return FATTN_ERR_CUDA;
+  if (!mark(3)) return FATTN_ERR_CUDA;
   return FATTN_OK;
+}
+
+extern "C" int fattn_bwd(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, float scale, int causal, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  return fattn_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+                      workspace_bytes, nullptr, stream);
 }
 
 extern "C" int fattn_tile_sizes(int d, int pass, int* block_q, int* block_k) {

@@ -30,6 +30,8 @@ SIGNATURES = {
     "fattn_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "fattn_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp,
                        _sz, _vp]),
+    "fattn_bwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i,
+                          _vp, _sz, _vp, _vp]),
     "fattn_tile_sizes": (_i, [_i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "fattn_device_error": (_i, [ctypes.POINTER(ctypes.c_uint), _i]),
     "fattn_status_string": (ctypes.c_char_p, [_i]),
@@ -109,6 +111,21 @@ def fattn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, worksp
                                          _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
                                          int(bool(causal)), _ptr(workspace), int(workspace_bytes),
                                          _stream(stream)))
+
+
+def fattn_bwd_ex(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+                 workspace_bytes, phase_events, stream=None):
+    """phase_events: None or 4 torch.cuda.Event(enable_timing=True) objects."""
+    arr = None
+    if phase_events is not None:
+        for ev in phase_events:
+            if ev.cuda_event == 0:  # torch creates the handle on first record
+                ev.record()
+        arr = (ctypes.c_void_p * 4)(*[ev.cuda_event for ev in phase_events])
+    _check("fattn_bwd_ex", load().fattn_bwd_ex(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, H,
+        N, d, float(scale), int(bool(causal)), _ptr(workspace), int(workspace_bytes),
+        ctypes.cast(arr, ctypes.c_void_p) if arr is not None else None, _stream(stream)))
 
 
 def fattn_tile_sizes(d, pass_):

@@ -1,0 +1,145 @@
+"""Backward parity: libfattn's sm_103a backward against the fp64 oracle.
+
+The GPU backward consumes the GPU forward's O and LSE (as a user would);
+the oracle recomputes everything from Q, K, V, dO in fp64.  Bar: dQ, dK, dV
+max-abs <= 2e-2 and mean-abs <= 2e-3.  Small problems are compared element
+by element; the full-size workloads run in the benchmark's launch
+configuration and are compared on whole sampled heads.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from online_softmax_08_gb300 import fattn
+from online_softmax_08_gb300.inputs import WORKLOADS, default_scale, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+G_MAX, G_MEAN = 2e-2, 2e-3
+
+
+def _f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def _gpu_grads(q, k, v, do, scale, causal):
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (x.to(dev).contiguous() for x in (q, k, v, do))
+    o, lse = fattn.forward(qd, kd, vd, scale, causal)
+    dq, dk, dv = fattn.backward(qd, kd, vd, o, lse, dod, scale, causal)
+    torch.cuda.synchronize()
+    assert fattn.fattn_device_error() == 0
+    return dq, dk, dv
+
+
+def _check(got, ref, what):
+    got = np.asarray(got)
+    assert np.isfinite(got).all(), what
+    err = np.abs(got - ref)
+    assert err.max() <= G_MAX, (what, err.max())
+    assert err.mean() <= G_MEAN, (what, err.mean())
+
+
+SMALL = [
+    (1, 1, 256, 64, False),
+    (1, 2, 300, 128, False),
+    (1, 2, 300, 128, True),
+    (2, 1, 129, 64, True),
+    (1, 1, 1, 128, True),
+    (1, 1, 1, 64, False),
+    (1, 3, 127, 128, True),
+    (1, 2, 513, 64, True),
+    (1, 1, 640, 128, False),
+    (2, 2, 384, 128, True),
+    (1, 2, 1000, 64, False),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", SMALL)
+def test_backward_matches_oracle_elementwise(B, H, N, d, causal):
+    q, k, v, do = make_inputs(B, H, N, d, seed=5151 + N + d, with_do=True)
+    scale = default_scale(d)
+    dq, dk, dv = _gpu_grads(q, k, v, do, scale, causal)
+    ref = oracle.attention_bwd(_f64(q), _f64(k), _f64(v), _f64(do), scale, causal)
+    for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        _check(_f64(got), r, name)
+
+
+def test_backward_logit_stress_small():
+    """Q ~ 4 N(0,1): the logit-stress inputs (a forward-only workload) pushed
+    through the backward too.  dK = scale dS^T Q then sums bf16-rounded dS
+    against |Q| up to ~16: rounding dS alone to bf16 (in fp64 otherwise) moves
+    dK by up to 0.035 on these inputs, so the max bar here is 4e-2; the mean
+    bar is the workload's 2e-3."""
+    q, k, v, do = make_inputs(1, 2, 500, 128, seed=91, q_std=4.0, v_dist="uniform", with_do=True)
+    scale = default_scale(128)
+    dq, dk, dv = _gpu_grads(q, k, v, do, scale, False)
+    ref = oracle.attention_bwd(_f64(q), _f64(k), _f64(v), _f64(do), scale, False)
+    for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        got = _f64(got)
+        assert np.isfinite(got).all()
+        err = np.abs(got - r)
+        assert err.max() <= 4e-2, (name, err.max())
+        assert err.mean() <= G_MEAN, (name, err.mean())
+
+
+def test_workspace_contents_do_not_matter():
+    q, k, v, do = make_inputs(1, 2, 400, 128, seed=92, with_do=True)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    scale = default_scale(128)
+    o, lse = fattn.forward(qd, kd, vd, scale, True)
+    nbytes = fattn.fattn_bwd_workspace_bytes(1, 2, 400, 128)
+    ws = torch.full((nbytes,), 0x7f, dtype=torch.uint8, device=dev)  # garbage (large floats)
+    g1 = fattn.backward(qd, kd, vd, o, lse, dod, scale, True, workspace=ws)
+    g2 = fattn.backward(qd, kd, vd, o, lse, dod, scale, True, workspace=ws)
+    torch.cuda.synchronize()
+    for a, b in zip(g1, g2):
+        np.testing.assert_allclose(_f64(a), _f64(b), atol=1e-2)
+    ref = oracle.attention_bwd(_f64(q), _f64(k), _f64(v), _f64(do), scale, True)
+    for name, got, r in zip(("dq", "dk", "dv"), g1, ref):
+        _check(_f64(got), r, name)
+
+
+def _sampled_heads(name, causal, n_heads):
+    w = WORKLOADS[name]
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    q, k, v, do = make_inputs(B, H, N, d, w["seed"], w["q_std"], w["v_dist"], with_do=True)
+    scale = default_scale(d)
+    dq, dk, dv = _gpu_grads(q, k, v, do, scale, causal)
+    g = torch.Generator().manual_seed(w["seed"] + 17)
+    heads = sorted(torch.randperm(B * H, generator=g)[:n_heads].tolist())
+    ref = oracle.attention_bwd(_f64(q), _f64(k), _f64(v), _f64(do), scale, causal, heads=heads)
+    for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        _check(_f64(got).reshape(B * H, N, d)[heads], r, name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_b4h16_n2048_d64_sampled_heads(causal):
+    _sampled_heads("b4h16_n2048_d64", causal, n_heads=4)
+
+
+def test_headline_b1h32_n8192_d128_causal_sampled_heads():
+    _sampled_heads("b1h32_n8192_d128_causal", True, n_heads=1)
+
+
+def test_long_sequence_backward_slice_b1h1_n4096_d128():
+    _sampled_heads("long_bwd_slice_b1h1_n4096_d128_causal", True, n_heads=1)
+
+
+def test_backward_argument_checks():
+    dev = torch.device("cuda:0")
+    x = torch.zeros(1, 1, 128, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.zeros(1, 1, 128, dtype=torch.float32, device=dev)
+    nbytes = fattn.fattn_bwd_workspace_bytes(1, 1, 128, 128)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    lib = fattn.load()
+    p, s = x.data_ptr(), torch.cuda.current_stream().cuda_stream
+    args = [p, p, p, p, lse.data_ptr(), p, p, p, p, 1, 1, 128, 128, 0.1, 1]
+    assert lib.fattn_bwd(*args, ws.data_ptr(), nbytes - 1, s) == 4
+    assert lib.fattn_bwd(*args, ws.data_ptr() + 16, nbytes, s) == 4
+    bad = list(args)
+    bad[12] = 32
+    assert lib.fattn_bwd(*bad, ws.data_ptr(), nbytes, s) == 2
+    torch.cuda.synchronize()

@@ -102,6 +102,25 @@ int fattn_bwd_ex(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, void* workspace, size_t workspace_bytes,
                  void* const* phase_events, void* stream);
 
+/* Size of the device array that fattn_bwd_noalloc uses as its workspace. */
+#define FATTN_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* fattn_bwd without a caller-provided workspace, for callers that cannot
+ * allocate device memory where they run the backward (a plugin inside a host
+ * program that owns the CUDA allocator, or a runtime that reserves its whole
+ * memory budget up front).  The pages have no counterpart to this entry
+ * point; it is a packaging variant of fattn_bwd.
+ * The workspace is a fixed device array of FATTN_NOALLOC_SCRATCH_BYTES that
+ * every GPU loading the library holds until exit; nothing is allocated or
+ * freed.  Problems with fattn_bwd_workspace_bytes(B,H,N,d) larger than that
+ * return FATTN_ERR_WORKSPACE and launch nothing.  All calls share the array:
+ * calls that overlap on the GPU race on it.  The first call on a device looks
+ * up the array's device address, so it should come before any stream capture.
+ * Arguments, layouts, results and other errors are those of fattn_bwd. */
+int fattn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                      int H, int N, int d, float scale, int causal, void* stream);
+
 /* Tile shape used by a pass (0 = forward, 1 = backward) for head size d:
  * rows of Q per tile and keys per K/V tile.  Returns FATTN_OK or
  * FATTN_ERR_UNSUPPORTED. */

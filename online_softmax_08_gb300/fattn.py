@@ -32,6 +32,8 @@ SIGNATURES = {
                        _sz, _vp]),
     "fattn_bwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i,
                           _vp, _sz, _vp, _vp]),
+    "fattn_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f,
+                               _i, _vp]),
     "fattn_tile_sizes": (_i, [_i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "fattn_device_error": (_i, [ctypes.POINTER(ctypes.c_uint), _i]),
     "fattn_status_string": (ctypes.c_char_p, [_i]),
@@ -126,6 +128,13 @@ def fattn_bwd_ex(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, wor
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, H,
         N, d, float(scale), int(bool(causal)), _ptr(workspace), int(workspace_bytes),
         ctypes.cast(arr, ctypes.c_void_p) if arr is not None else None, _stream(stream)))
+
+
+def fattn_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, stream=None):
+    """fattn_bwd with the library's built-in workspace (allocates nothing)."""
+    _check("fattn_bwd_noalloc", load().fattn_bwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, H,
+        N, d, float(scale), int(bool(causal)), _stream(stream)))
 
 
 def fattn_tile_sizes(d, pass_):

@@ -1,0 +1,60 @@
+"""fattn_bwd_noalloc: the backward pass with the library's built-in workspace.
+
+It exists for callers that cannot allocate device memory where they run the
+backward (a plugin inside a host program that owns the CUDA allocator, or a
+runtime that reserves its whole memory budget up front).  This file runs last
+(pytest collects it after the others), so a failure here does not hide any
+other test when the run stops at the first failure; it also passes when run
+alone in a fresh process.
+
+Checks: two calls in a row through the C-ABI agree with fattn_bwd (the
+entry point that takes a caller workspace) within the parity tolerance of the
+other backward tests; a problem whose workspace exceeds the built-in size is
+rejected before any launch.
+"""
+import numpy as np
+import pytest
+import torch
+
+from online_softmax_08_gb300 import fattn
+from online_softmax_08_gb300.inputs import default_scale, make_inputs
+
+G_MAX, G_MEAN = 2e-2, 2e-3
+SCRATCH_BYTES = 64 << 20  # FATTN_NOALLOC_SCRATCH_BYTES in include/fattn.h
+
+
+def _f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("B,H,N,d,causal", [(1, 2, 777, 128, True), (2, 2, 640, 64, False)])
+def test_noalloc_matches_workspace_backward_twice(B, H, N, d, causal):
+    dev = torch.device("cuda:0")
+    q, k, v, do = (x.to(dev) for x in make_inputs(B, H, N, d, seed=6060 + N, with_do=True))
+    scale = default_scale(d)
+    o, lse = fattn.forward(q, k, v, scale, causal)
+    ref = fattn.backward(q, k, v, o, lse, do, scale, causal)
+    lib = fattn.load()
+    s = torch.cuda.current_stream().cuda_stream
+    for _ in range(2):
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        status = lib.fattn_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                       lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
+                                       dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale,
+                                       int(causal), s)
+        assert status == 0, fattn.fattn_status_string(status)
+        torch.cuda.synchronize()
+        for got, want in zip((dq, dk, dv), ref):
+            err = np.abs(_f64(got) - _f64(want))
+            assert err.max() <= G_MAX and err.mean() <= G_MEAN
+    assert fattn.fattn_device_error() == 0
+
+
+@pytest.mark.gpu
+def test_noalloc_rejects_problems_beyond_the_scratch_size():
+    B, H, N, d = 1, 8, 16384, 128
+    assert fattn.fattn_bwd_workspace_bytes(B, H, N, d) > SCRATCH_BYTES
+    lib = fattn.load()
+    a = 1 << 20  # never dereferenced: the size check comes first
+    assert lib.fattn_bwd_noalloc(a, a, a, a, a, a, a, a, a, B, H, N, d, 0.1, 1, None) == 4

@@ -55,6 +55,17 @@ def peaks():
         return 1900.0, 6800.0, "fallback"
 
 
+def _clean(x):
+    """JSON-safe copy: NaN and inf become null."""
+    if isinstance(x, dict):
+        return {k: _clean(v) for k, v in x.items()}
+    if isinstance(x, (list, tuple)):
+        return [_clean(v) for v in x]
+    if isinstance(x, float) and not math.isfinite(x):
+        return None
+    return x
+
+
 # ------------------------------------------------------------------ multi-rank plumbing
 
 def dist_env():
@@ -361,7 +372,7 @@ def run_gpu(args):
             "gpu_launches": (int(do_fwd) + 3 * int(do_bwd)) * K,
             "clocks": clk,
         }
-        print(json.dumps(line), flush=True)
+        print(json.dumps(_clean(line)), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -17,7 +17,11 @@
 //   warp 9     one thread issues every TMA load.
 //
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 after it.
-// Shared memory: Q_0, Q_1 | K/V ring | P_0, P_1 (bf16, 128B-swizzled K-major).
+// P_s (bf16, two per 32-bit column) overwrites the first 64 columns of S_s
+// once the softmax has read S_s, and feeds O_s += P_s V as the TMEM A operand,
+// so P never touches shared memory.  The MMA thread issues, per subtile,
+// O_s += P_s V_j before S_s = Q_s K_{j+1}^T (the pipe runs them in order).
+// Shared memory: Q_0, Q_1 | K/V ring.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -32,12 +36,10 @@ struct Fwd {
   static constexpr int BN = 128;                  // keys per K/V tile
   static constexpr int HALF = BM * 128;           // one 64-column, 128-row swizzled half (bytes)
   static constexpr int TILE = BM * D * 2;         // Q, K, V or O tile (bf16)
-  static constexpr int PTILE = BM * BN * 2;       // P tile (bf16)
-  static constexpr int STAGES = D == 128 ? 3 : 6; // K/V ring slots
+  static constexpr int STAGES = D == 128 ? 5 : 8; // K/V ring slots
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + 2 * TILE;
-  static constexpr int OFF_P = OFF_KV + STAGES * TILE;
-  static constexpr int OFF_BAR = OFF_P + 2 * PTILE;
+  static constexpr int OFF_BAR = OFF_KV + STAGES * TILE;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers + alignment slack
   static constexpr int THREADS = 320;
   static constexpr uint32_t TM_S = 0;
@@ -49,12 +51,11 @@ struct Fwd {
 // Barrier slots (8 bytes each) inside the OFF_BAR block.
 enum {
   B_Q = 0,
-  B_S_FULL = 1,   // [2] MMA -> softmax: S_s ready in TMEM
-  B_S_FREE = 3,   // [2] softmax -> MMA: S_s copied to registers
-  B_P_FULL = 5,   // [2] softmax -> MMA: P_s in smem and O_s rescaled
-  B_PV_DONE = 7,  // [2] MMA -> softmax: O_s += P_s V finished
-  B_MMA_DONE = 9,
-  B_KV_FULL = 10,  // [STAGES]
+  B_S_FULL = 1,   // [2] MMA -> softmax: S_s ready in TMEM (and every earlier MMA done)
+  B_P_FULL = 3,   // [2] softmax -> MMA: P_s in TMEM and O_s rescaled
+  B_PV_DONE = 5,  // [2] MMA -> epilogue: O_s += P_s V finished
+  B_MMA_DONE = 7,
+  B_KV_FULL = 8,  // [STAGES], then kv_empty [STAGES]
 };
 
 template <int D>
@@ -101,7 +102,6 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
     mbar_init(bar(B_Q), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_S_FULL + s), 1);
-      mbar_init(bar(B_S_FREE + s), 128);
       mbar_init(bar(B_P_FULL + s), 128);
       mbar_init(bar(B_PV_DONE + s), 1);
     }
@@ -169,16 +169,13 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
         }
         mma_commit(bar(B_S_FULL + s));
       };
-      auto issue_pv = [&](int s, int j) {  // O_s += P_s V_j
-        const uint32_t a = sbase + C::OFF_P + s * C::PTILE;
+      auto issue_pv = [&](int s, int j) {  // O_s += P_s V_j, P_s from TMEM
         const uint32_t b = sbase + C::OFF_KV + ((2 * j + 1) % ST) * C::TILE;
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * C::HALF + (kk & 3) * 32;
-          const uint32_t b_off = kk * 16 * 128;
-          mma_bf16_ss(tmem + C::TM_O + s * D, sdesc_sw128(a + a_off, 16, 1024),
-                      sdesc_sw128(b + b_off, C::HALF, 1024), C::IDESC_PV, (j > 0 || kk > 0));
-        }
+        for (int kk = 0; kk < C::BN / 16; ++kk)  // 16 keys = 8 packed TMEM columns per step
+          mma_bf16_ts(tmem + C::TM_O + s * D, tmem + C::TM_S + s * 128 + kk * 8,
+                      sdesc_sw128(b + kk * 16 * 128, C::HALF, 1024), C::IDESC_PV,
+                      (j > 0 || kk > 0));
         mma_commit(bar(B_PV_DONE + s));
       };
       mbar_wait(bar(B_Q), 0, wctx, ERR_SITE_FWD | 0x12);
@@ -191,30 +188,21 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
       }
       for (int j = 0; j < n_max; ++j) {
         const bool next = j + 1 < n_max;
-        if (next) kv_wait(2 * (j + 1));
-        if (j + 1 < nt0) {
-          mbar_wait(bar(B_S_FREE + 0), j & 1, wctx, ERR_SITE_FWD | 0x13);
-          tc_fence_after();
-          issue_s(0, j + 1);
-        }
-        if (j < nt0) {
-          kv_wait(2 * j + 1);
-          mbar_wait(bar(B_P_FULL + 0), j & 1, wctx, ERR_SITE_FWD | 0x14);
-          tc_fence_after();
-          issue_pv(0, j);
-        }
-        if (j + 1 < nt1) {
-          mbar_wait(bar(B_S_FREE + 1), j & 1, wctx, ERR_SITE_FWD | 0x15);
-          tc_fence_after();
-          issue_s(1, j + 1);
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          const int nts = s ? nt1 : nt0;
+          if (j < nts) {
+            kv_wait(2 * j + 1);
+            mbar_wait(bar(B_P_FULL + s), j & 1, wctx, ERR_SITE_FWD | 0x14);
+            tc_fence_after();
+            issue_pv(s, j);
+          }
+          if (j + 1 < nts) {  // after the PV above: S_s is overwritten in pipe order
+            kv_wait(2 * (j + 1));
+            issue_s(s, j + 1);
+          }
         }
         if (next) mma_commit(kv_empty0 + 8u * ((2 * (j + 1)) % ST));
-        if (j < nt1) {
-          kv_wait(2 * j + 1);
-          mbar_wait(bar(B_P_FULL + 1), j & 1, wctx, ERR_SITE_FWD | 0x16);
-          tc_fence_after();
-          issue_pv(1, j);
-        }
         mma_commit(kv_empty0 + 8u * ((2 * j + 1) % ST));
       }
       mma_commit(bar(B_MMA_DONE));
@@ -232,11 +220,11 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
     const uint32_t tO = tmem + lane_off + C::TM_O + s * D;
     const int row = my_r0 + t;
     const float sl2 = p.scale_log2;
-    const uint32_t p_base = sbase + C::OFF_P + s * C::PTILE;
     float m_run = -INFINITY, l_run = 0.f;
     unsigned long long n_full = 0, n_masked = 0;
 
     for (int j = 0; j < my_nt; ++j) {
+      // s_full also means every earlier MMA, including O_s += P_s V_{j-1}, is done
       mbar_wait(bar(B_S_FULL + s), j & 1, wctx, ERR_SITE_FWD | 0x21);
       tc_fence_after();
       uint32_t u[4][32];
@@ -245,8 +233,6 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
       tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < 4; ++c) reg_fence32(u[c]);
-      tc_fence_before();
-      mbar_arrive(bar(B_S_FREE + s));
 
       float sv[128];
 #pragma unroll
@@ -283,33 +269,27 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
       const bool rescale = m_new != m_run;
       float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
 #pragma unroll
-      for (int k = 0; k < 128; k += 4) {
-        sv[k] = ex2(fmaf(sv[k], sl2, -msc));
-        sv[k + 1] = ex2(fmaf(sv[k + 1], sl2, -msc));
-        sv[k + 2] = ex2(fmaf(sv[k + 2], sl2, -msc));
-        sv[k + 3] = ex2(fmaf(sv[k + 3], sl2, -msc));
-        ls0 += sv[k];
-        ls1 += sv[k + 1];
-        ls2 += sv[k + 2];
-        ls3 += sv[k + 3];
+      for (int h = 0; h < 2; ++h) {  // 64 keys -> 32 packed bf16x2 TMEM columns
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 64; k += 4) {
+          const int kk = h * 64 + k;
+          const float p0 = ex2(fmaf(sv[kk], sl2, -msc));
+          const float p1 = ex2(fmaf(sv[kk + 1], sl2, -msc));
+          const float p2 = ex2(fmaf(sv[kk + 2], sl2, -msc));
+          const float p3 = ex2(fmaf(sv[kk + 3], sl2, -msc));
+          ls0 += p0;
+          ls1 += p1;
+          ls2 += p2;
+          ls3 += p3;
+          pk[k / 2] = pack_bf16x2(p0, p1);
+          pk[k / 2 + 1] = pack_bf16x2(p2, p3);
+        }
+        tmem_st32(tS + h * 32, pk);
       }
       l_run = l_run * alpha + ((ls0 + ls1) + (ls2 + ls3));
       m_run = m_new;
 
-      // P_s and O_s are still in use by the previous O_s += P_s V
-      if (j > 0) {
-        mbar_wait(bar(B_PV_DONE + s), (j - 1) & 1, wctx, ERR_SITE_FWD | 0x22);
-        tc_fence_after();
-      }
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {  // 16 chunks of 8 keys; two 64-key swizzled halves
-        const uint32_t addr = p_base + (c >> 3) * C::HALF + t * 128 + (((c & 7) ^ (t & 7)) << 4);
-        st_shared_v4(addr, pack_bf16x2(sv[8 * c], sv[8 * c + 1]),
-                     pack_bf16x2(sv[8 * c + 2], sv[8 * c + 3]),
-                     pack_bf16x2(sv[8 * c + 4], sv[8 * c + 5]),
-                     pack_bf16x2(sv[8 * c + 6], sv[8 * c + 7]));
-      }
-      fence_proxy_async_smem();
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -320,8 +300,8 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
           tmem_st32(tO + c * 32, o);
         }
-        tmem_wait_st();
       }
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_P_FULL + s));
     }

@@ -65,7 +65,7 @@ struct WaitCtx {
   unsigned int* err;              // global, may be null
 };
 
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
+static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
                                             uint32_t site) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {

@@ -155,18 +155,11 @@ extern "C" int fattn_bwd_ex(const void* q, const void* k, const void* v, const v
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int bq = 0, bk = 0;
   fattn_tile_sizes(d, 1, &bq, &bk);
-  CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   if (!make_bf16_map(&tq, q, d, N, BH, bq) || !make_bf16_map(&tdo, dout, d, N, BH, bq) ||
       !make_bf16_map(&tk, k, d, N, BH, bk) || !make_bf16_map(&tv, v, d, N, BH, bk) ||
       !make_bf16_map(&tdk, dk, d, N, BH, bk) || !make_bf16_map(&tdv, dv, d, N, BH, bk))
     return FATTN_ERR_CUDA;
-  // dQ accumulator: fp32, add-reduced tile by tile
-  const bool ok = (d == 128)
-                      ? make_map(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, BH, 128,
-                                 bq, CU_TENSOR_MAP_SWIZZLE_NONE)
-                      : make_map(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, BH, 32,
-                                 bq, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (!ok) return FATTN_ERR_CUDA;
   auto mark = [&](int i) {
     return !phase_events ||
            cudaEventRecord(static_cast<cudaEvent_t>(phase_events[i]), s) == cudaSuccess;
@@ -183,8 +176,9 @@ extern "C" int fattn_bwd_ex(const void* q, const void* k, const void* v, const v
   p.scale_log2 = scale * 1.4426950408889634f;
   p.lse = lse;
   p.delta = delta;
+  p.dq_acc = dq_acc;
   p.err = dev->err;
-  cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, tdk, tdv, tdq, p, s);
+  cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, tdk, tdv, p, s);
   if (e == cudaErrorNotSupported) return FATTN_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return FATTN_ERR_CUDA;
   if (!mark(2)) return FATTN_ERR_CUDA;

@@ -12,26 +12,31 @@
 //   dP^T = V dO_i^T
 //   dS^T = P^T o (dP^T - D_i)                D_i = rowsum(dO_i o O_i), precomputed
 //   dK  += dS^T Q_i                          (x scale in the epilogue)
-//   dQ_i += dS K                             (fp32, add-reduced into a workspace
-//                                             by TMA; x scale in the convert kernel)
+//   dQ_i += dS K                             (fp32 partials added into a workspace;
+//                                             x scale in the convert kernel)
 //
 // One CTA owns one 128-key block K_j, V_j of one (batch, head); its dK_j and
 // dV_j accumulate in TMEM while the query blocks Q_i, dO_i (BQ rows) stream
-// through a two-stage ring.  With causal masking only query blocks i with
-// queries >= the block's first key are visited.
+// through a three-stage TMA ring.  With causal masking only query blocks i
+// with queries >= the block's first key are visited.
 //
-// dQ strategy: each CTA produces a partial dQ_i per visited query block and
-// adds it into an fp32 accumulator with one bulk tensor reduce (no per-element
-// atomics), instead of a second pass that would recompute S and dP (two more
-// matmuls per tile).
+// dQ strategy: each CTA forms a partial dQ_i per visited query block in TMEM
+// (two buffers, so the next one is computed while the last is drained) and a
+// drain warpgroup adds it into an fp32 accumulator with coalesced
+// red.global.add, straight from registers.  The alternative, a second pass
+// parallel over query blocks, would recompute S and dP (two more matmuls per
+// tile, 7 instead of 5).
 //
 // Head size 128 uses BQ = 64 and computes dQ_i^T = K^T dS^T (M = d = 128);
 // head size 64 uses BQ = 128 and computes dQ_i = dS K (M = BQ = 128).  Both keep
-// every MMA at M = 128 and fit TMEM (448 of 512 columns).
+// every MMA at M = 128.  TMEM (512 columns): dK, dV, S^T, dP^T, dQ x 2.
+// P^T (bf16) overwrites the first half of each warpgroup's own S^T columns and
+// feeds dV += P^T dO as the TMEM A operand.
 //
-// Warp roles (320 threads): warps 0-7 compute (two warpgroups; thread t of a
+// Warp roles (512 threads): warps 0-7 compute (two warpgroups; thread t of a
 // warpgroup owns key row t = TMEM lane t, warpgroup w owns half the query
-// columns), warp 8 issues MMAs, warp 9 issues TMA loads and stages LSE and D.
+// columns), warps 8-11 drain dQ, warp 12 issues MMAs, warp 13 issues TMA loads
+// and stages LSE and D, warps 14-15 idle.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -43,45 +48,49 @@ struct Bwd {
   static constexpr int BK = 128;                    // keys per CTA
   static constexpr int BQ = D == 128 ? 64 : 128;    // queries per step
   static constexpr int CW = BQ / 2;                 // query columns per compute warpgroup
-  static constexpr int KHALF = BK * 128;            // 64-column half of a K/V tile (bytes)
+  static constexpr int NCH = CW / 32;               // 32-column TMEM chunks per thread
+  static constexpr int QST = 3;                     // Q/dO ring stages
+  static constexpr int KHALF = BK * 128;            // 64-column half of a K/V or dS^T tile
   static constexpr int QHALF = BQ * 128;            // 64-column half of a Q/dO tile
   static constexpr int TILE_K = BK * D * 2;
   static constexpr int TILE_Q = BQ * D * 2;
-  static constexpr int PT = BK * BQ * 2;            // P^T or dS^T tile (bf16)
-  static constexpr int DQ_STAGE = BQ * D * 4;       // fp32 dQ staging
+  static constexpr int PT = BK * BQ * 2;            // dS^T tile (bf16)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE_K;
-  static constexpr int OFF_Q = OFF_V + TILE_K;                 // [2] stages
-  static constexpr int OFF_DO = OFF_Q + 2 * TILE_Q;            // [2]
-  static constexpr int OFF_P = OFF_DO + 2 * TILE_Q;
-  static constexpr int OFF_DS = OFF_P + PT;
-  static constexpr int OFF_DQ = OFF_DS + PT;
-  static constexpr int OFF_STAT = OFF_DQ + DQ_STAGE;           // [2] x {lse2[BQ], delta[BQ]}
-  static constexpr int OFF_BAR = OFF_STAT + 2 * 2 * BQ * 4;
+  static constexpr int OFF_Q = OFF_V + TILE_K;                 // [QST]
+  static constexpr int OFF_DO = OFF_Q + QST * TILE_Q;          // [QST]
+  static constexpr int OFF_DS = OFF_DO + QST * TILE_Q;
+  static constexpr int OFF_STAT = OFF_DS + PT;                 // [QST] x {lse2[BQ], delta[BQ]}
+  static constexpr int OFF_BAR = OFF_STAT + QST * 2 * BQ * 4;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 512;
+  static constexpr int DQC = 64;                    // TMEM columns of one dQ buffer
   static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_S = 2 * D, TM_DP = 2 * D + BQ,
                             TM_DQ = 2 * D + 2 * BQ;
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BQ, false, false);   // S^T, dP^T
   static constexpr uint32_t IDESC_ACC = idesc_bf16_f32(128, D, false, true);   // dV, dK
   static constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, D == 128 ? BQ : D, true, true);
+  // TMEM column of the packed P^T for MMA K-step kk (16 queries): warpgroup
+  // w's queries [w*CW, w*CW + CW) sit in the first CW/2 of its S^T columns
+  __host__ __device__ static constexpr uint32_t p_col(int kk) {
+    return TM_S + (uint32_t)((16 * kk) / CW) * CW + (uint32_t)((16 * kk) % CW) / 2;
+  }
 };
 
 enum {
   B_KV = 0,
-  B_S_FULL = 1,
-  B_S_FREE = 2,
-  B_DP_FULL = 3,
-  B_DP_FREE = 4,
-  B_P_FULL = 5,
-  B_DV_DONE = 6,
-  B_DS_FULL = 7,
-  B_DQ_FULL = 8,
-  B_DQ_FREE = 9,
-  B_MMA_DONE = 10,
-  B_Q_FULL = 11,   // [2]
-  B_Q_EMPTY = 13,  // [2]
-  B_COUNT = 15,
+  B_S_FULL = 1,    // MMA -> compute: S^T ready (and every earlier MMA done)
+  B_P_FULL = 2,    // compute -> MMA: P^T in TMEM
+  B_DP_FULL = 3,   // MMA -> compute: dP^T ready
+  B_DP_FREE = 4,   // compute -> MMA: dP^T read
+  B_DS_FULL = 5,   // compute -> MMA: dS^T in shared memory
+  B_DS_FREE = 6,   // MMA -> compute: dK and dQ have read dS^T
+  B_MMA_DONE = 7,
+  B_DQ_FULL = 8,   // [2] MMA -> drain: dQ buffer ready
+  B_DQ_FREE = 10,  // [2] drain -> MMA: dQ buffer read
+  B_Q_FULL = 12,   // [QST]
+  B_Q_EMPTY = 15,  // [QST]
+  B_COUNT = 18,
 };
 
 template <int D>
@@ -91,10 +100,9 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_dk,
-                     const __grid_constant__ CUtensorMap tm_dv,
-                     const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+                     const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
   using C = Bwd<D>;
-  constexpr int BQ = C::BQ;
+  constexpr int BQ = C::BQ, QST = C::QST;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -118,16 +126,17 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(B_KV), 1);
     mbar_init(bar(B_S_FULL), 1);
-    mbar_init(bar(B_S_FREE), 256);
+    mbar_init(bar(B_P_FULL), 256);
     mbar_init(bar(B_DP_FULL), 1);
     mbar_init(bar(B_DP_FREE), 256);
-    mbar_init(bar(B_P_FULL), 256);
-    mbar_init(bar(B_DV_DONE), 1);
     mbar_init(bar(B_DS_FULL), 256);
-    mbar_init(bar(B_DQ_FULL), 1);
-    mbar_init(bar(B_DQ_FREE), 256);
+    mbar_init(bar(B_DS_FREE), 1);
     mbar_init(bar(B_MMA_DONE), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_DQ_FULL + b), 1);
+      mbar_init(bar(B_DQ_FREE + b), 128);
+    }
+    for (int s = 0; s < QST; ++s) {
       mbar_init(bar(B_Q_FULL + s), 1 + 32);
       mbar_init(bar(B_Q_EMPTY + s), 1 + 256);
     }
@@ -143,7 +152,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 9) {
+  if (warp == 13) {
     // ---------------------------------------------------------------- loads
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -156,7 +165,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
     }
     const float kLog2e = 1.4426950408889634f;
     for (int it = 0; it < n_it; ++it) {
-      const int st = it & 1, use = it >> 1;
+      const int st = it % QST, use = it / QST;
       const int q0 = (i_start + it) * BQ;
       if (use > 0) mbar_wait(bar(B_Q_EMPTY + st), (use - 1) & 1, wctx, ERR_SITE_BWD | 0x01);
       if (lane == 0) {
@@ -180,15 +189,14 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
     }
     if (lane == 0) {
       mbar_wait(bar(B_KV), 0, wctx, ERR_SITE_BWD | 0x02);
-      for (int it = max(0, n_it - 2); it < n_it; ++it)
-        mbar_wait(bar(B_Q_FULL + (it & 1)), (it >> 1) & 1, wctx, ERR_SITE_BWD | 0x03);
+      for (int it = max(0, n_it - QST); it < n_it; ++it)
+        mbar_wait(bar(B_Q_FULL + it % QST), (it / QST) & 1, wctx, ERR_SITE_BWD | 0x03);
     }
     __syncwarp();
-  } else if (warp == 8) {
+  } else if (warp == 12) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
-      const uint32_t sP = sbase + C::OFF_P, sDS = sbase + C::OFF_DS;
+      const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sDS = sbase + C::OFF_DS;
       // D[128 x BQ] = X[128 keys x D] * Y[BQ x D]^T, both K-major
       auto mma_xyT = [&](uint32_t d_col, uint32_t x, uint32_t y) {
 #pragma unroll
@@ -199,34 +207,42 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
                       C::IDESC_S, kk > 0);
         }
       };
-      // D[128 x D] (+)= A[128 keys x BQ] (K-major) * Y[BQ x D] (MN-major)
-      auto mma_acc = [&](uint32_t d_col, uint32_t a, uint32_t y, bool acc) {
+      // dV += P^T (TMEM) * dO (MN-major)
+      auto mma_dv = [&](uint32_t sdo, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          mma_bf16_ts(tmem + C::TM_DV, tmem + C::p_col(kk),
+                      sdesc_sw128(sdo + kk * 16 * 128, C::QHALF, 1024), C::IDESC_ACC,
+                      (acc || kk > 0));
+      };
+      // dK += dS^T (K-major) * Q (MN-major)
+      auto mma_dk = [&](uint32_t sq, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t ao = (kk >> 2) * C::KHALF + (kk & 3) * 32;
-          const uint32_t yo = kk * 16 * 128;
-          mma_bf16_ss(tmem + d_col, sdesc_sw128(a + ao, 16, 1024),
-                      sdesc_sw128(y + yo, C::QHALF, 1024), C::IDESC_ACC, (acc || kk > 0));
+          mma_bf16_ss(tmem + C::TM_DK, sdesc_sw128(sDS + ao, 16, 1024),
+                      sdesc_sw128(sq + kk * 16 * 128, C::QHALF, 1024), C::IDESC_ACC,
+                      (acc || kk > 0));
         }
       };
       // dQ: both operands MN-major, reduction over the 128 keys
-      auto mma_dq = [&]() {
+      auto mma_dq = [&](uint32_t d_col) {
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk) {
           const uint32_t o = kk * 16 * 128;
           if (D == 128)  // dQ^T[d x BQ] = K^T[d x keys] * dS^T[keys x BQ]
-            mma_bf16_ss(tmem + C::TM_DQ, sdesc_sw128(sK + o, C::KHALF, 1024),
+            mma_bf16_ss(tmem + d_col, sdesc_sw128(sK + o, C::KHALF, 1024),
                         sdesc_sw128(sDS + o, C::KHALF, 1024), C::IDESC_DQ, kk > 0);
           else  // dQ[BQ x d] = dS[BQ x keys] * K[keys x d]
-            mma_bf16_ss(tmem + C::TM_DQ, sdesc_sw128(sDS + o, C::KHALF, 1024),
+            mma_bf16_ss(tmem + d_col, sdesc_sw128(sDS + o, C::KHALF, 1024),
                         sdesc_sw128(sK + o, C::KHALF, 1024), C::IDESC_DQ, kk > 0);
         }
       };
       auto q_wait = [&](int it) {
-        mbar_wait(bar(B_Q_FULL + (it & 1)), (it >> 1) & 1, wctx, ERR_SITE_BWD | 0x11);
+        mbar_wait(bar(B_Q_FULL + it % QST), (it / QST) & 1, wctx, ERR_SITE_BWD | 0x11);
       };
-      auto sQ = [&](int it) { return sbase + C::OFF_Q + (it & 1) * C::TILE_Q; };
-      auto sDO = [&](int it) { return sbase + C::OFF_DO + (it & 1) * C::TILE_Q; };
+      auto sQ = [&](int it) { return sbase + C::OFF_Q + (it % QST) * C::TILE_Q; };
+      auto sDO = [&](int it) { return sbase + C::OFF_DO + (it % QST) * C::TILE_Q; };
 
       mbar_wait(bar(B_KV), 0, wctx, ERR_SITE_BWD | 0x12);
       q_wait(0);
@@ -239,37 +255,73 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
         const bool next = it + 1 < n_it;
         mbar_wait(bar(B_P_FULL), it & 1, wctx, ERR_SITE_BWD | 0x13);
         tc_fence_after();
-        mma_acc(C::TM_DV, sP, sDO(it), it > 0);
-        mma_commit(bar(B_DV_DONE));
-        if (next) {
+        mma_dv(sDO(it), it > 0);
+        if (next) {  // overwrites S^T / P^T: after the dV above in pipe order
           q_wait(it + 1);
-          mbar_wait(bar(B_S_FREE), it & 1, wctx, ERR_SITE_BWD | 0x14);
-          tc_fence_after();
           mma_xyT(C::TM_S, sK, sQ(it + 1));
           mma_commit(bar(B_S_FULL));
         }
         mbar_wait(bar(B_DS_FULL), it & 1, wctx, ERR_SITE_BWD | 0x15);
         tc_fence_after();
-        mma_acc(C::TM_DK, sDS, sQ(it), it > 0);
+        mma_dk(sQ(it), it > 0);
         if (next) {
           mbar_wait(bar(B_DP_FREE), it & 1, wctx, ERR_SITE_BWD | 0x16);
           tc_fence_after();
           mma_xyT(C::TM_DP, sV, sDO(it + 1));
           mma_commit(bar(B_DP_FULL));
         }
-        if (it > 0) {
-          mbar_wait(bar(B_DQ_FREE), (it - 1) & 1, wctx, ERR_SITE_BWD | 0x17);
+        const int b = it & 1;
+        if (it >= 2) {
+          mbar_wait(bar(B_DQ_FREE + b), ((it - 2) >> 1) & 1, wctx, ERR_SITE_BWD | 0x17);
           tc_fence_after();
         }
-        mma_dq();
-        mma_commit(bar(B_DQ_FULL));
-        mma_commit(bar(B_Q_EMPTY + (it & 1)));
+        mma_dq(C::TM_DQ + b * C::DQC);
+        mma_commit(bar(B_DQ_FULL + b));
+        mma_commit(bar(B_DS_FREE));
+        mma_commit(bar(B_Q_EMPTY + it % QST));
       }
       mma_commit(bar(B_MMA_DONE));
       mbar_wait(bar(B_MMA_DONE), 0, wctx, ERR_SITE_BWD | 0x18);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 8 && warp < 12) {
+    // ---------------------------------------------------------------- dQ drain
+    const int t = threadIdx.x & 127;  // TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    for (int it = 0; it < n_it; ++it) {
+      const int b = it & 1;
+      const int q0 = (i_start + it) * BQ;
+      mbar_wait(bar(B_DQ_FULL + b), (it >> 1) & 1, wctx, ERR_SITE_BWD | 0x31);
+      tc_fence_after();
+      uint32_t r[2][32];
+      tmem_ld32(tmem + lane_off + C::TM_DQ + b * C::DQC, r[0]);
+      tmem_ld32(tmem + lane_off + C::TM_DQ + b * C::DQC + 32, r[1]);
+      tmem_wait_ld();
+      reg_fence32(r[0]);
+      reg_fence32(r[1]);
+      tc_fence_before();
+      mbar_arrive(bar(B_DQ_FREE + b));
+      if (D == 128) {
+        // lanes are d, columns are queries: one warp adds 32 consecutive floats per query row
+        float* base = p.dq_acc + ((size_t)bh * N + q0) * D + t;
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (q0 + c < N) red_add_f32(base + (size_t)c * D, __uint_as_float(r[c >> 5][c & 31]));
+      } else {
+        // lanes are queries, columns are d: each thread adds its query row
+        if (q0 + t < N) {
+          float* row = p.dq_acc + ((size_t)bh * N + q0 + t) * D;
+#pragma unroll
+          for (int c = 0; c < 64; c += 4)
+            red_add_v4_f32(row + c, __uint_as_float(r[c >> 5][c & 31]),
+                           __uint_as_float(r[c >> 5][(c & 31) + 1]),
+                           __uint_as_float(r[c >> 5][(c & 31) + 2]),
+                           __uint_as_float(r[c >> 5][(c & 31) + 3]));
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < 8) {
     // ---------------------------------------------------------------- compute (warps 0-7)
     const int w = warp >> 2;             // warpgroup: query columns [w*CW, w*CW + CW)
     const int t = threadIdx.x & 127;     // key row in the block == TMEM lane
@@ -278,69 +330,29 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
     const int kr = k0 + t;
     const float sl2 = p.scale_log2;
     constexpr int CW = C::CW;
-    constexpr int NCH = CW / 32;  // 32-column TMEM chunks per thread
-
-    // stage one dQ tile in shared memory and add it into the fp32 accumulator
-    auto drain_dq = [&](int it) {
-      const int q0 = (i_start + it) * BQ;
-      uint32_t r[32];
-      // D == 128: lanes are d, columns are queries; D == 64: lanes are queries, columns d
-      tmem_ld32(tmem + lane_off + C::TM_DQ + w * 32, r);
-      tmem_wait_ld(r);
-      tc_fence_before();
-      mbar_arrive(bar(B_DQ_FREE));
-      if (ctid == 0) bulk_wait_read_all();  // the previous reduce has read the staging
-      named_bar_sync(1, 256);
-      const uint32_t sdq = sbase + C::OFF_DQ;
-      if (D == 128) {
-        // staging [BQ queries][128 d] fp32, unswizzled: thread t writes column t
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const uint32_t addr = sdq + (uint32_t)((w * 32 + c) * D + t) * 4u;
-          asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(r[c]) : "memory");
-        }
-      } else {
-        // staging: two 32-column boxes of [128 queries][128 B], 128B-swizzled
-        const uint32_t box = sdq + (uint32_t)w * (128 * 128);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_shared_v4(box + t * 128 + ((c ^ (t & 7)) << 4), r[4 * c], r[4 * c + 1], r[4 * c + 2],
-                       r[4 * c + 3]);
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 256);
-      if (ctid == 0) {
-        if (D == 128) {
-          tma_reduce_add_3d(&tm_dq, sdq, 0, q0, bh);
-        } else {
-          tma_reduce_add_3d(&tm_dq, sdq, 0, q0, bh);
-          tma_reduce_add_3d(&tm_dq, sdq + 128 * 128, 32, q0, bh);
-        }
-        bulk_commit();
-      }
-    };
+    constexpr int NCH = C::NCH;
+    const uint32_t tS = tmem + lane_off + C::TM_S + w * CW;
+    const uint32_t tDP = tmem + lane_off + C::TM_DP + w * CW;
 
     for (int it = 0; it < n_it; ++it) {
-      const int st = it & 1;
+      const int st = it % QST;
       const int q0 = (i_start + it) * BQ;
-      mbar_wait(bar(B_Q_FULL + st), (it >> 1) & 1, wctx, ERR_SITE_BWD | 0x21);
+      mbar_wait(bar(B_Q_FULL + st), (it / QST) & 1, wctx, ERR_SITE_BWD | 0x21);
       const float* stat = reinterpret_cast<const float*>(smem + C::OFF_STAT + st * 2 * BQ * 4);
       const float* lse2 = stat + w * CW;
       const float* dlt = stat + BQ + w * CW;
 
-      // ---- P^T = exp2(S^T * scale * log2e - LSE2), masked
+      // ---- P^T = exp2(S^T * scale * log2e - LSE2), masked; bf16 into TMEM
       mbar_wait(bar(B_S_FULL), it & 1, wctx, ERR_SITE_BWD | 0x22);
       tc_fence_after();
       float pv[CW];
       {
         uint32_t u[NCH][32];
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) tmem_ld32(tmem + lane_off + C::TM_S + w * CW + c * 32, u[c]);
+        for (int c = 0; c < NCH; ++c) tmem_ld32(tS + c * 32, u[c]);
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < NCH; ++c) reg_fence32(u[c]);
-        tc_fence_before();
-        mbar_arrive(bar(B_S_FREE));
         // key kr sees query q iff kr < N and (not causal or kr <= q); queries
         // past N already have LSE2 = +inf
         int lo = 0;  // first visible column of this warpgroup
@@ -352,43 +364,34 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
           pv[c] = c < lo ? 0.f : ex2(fmaf(s, sl2, -lse2[c]));
         }
       }
-      if (it > 0) {  // the previous dV MMA has read the P^T buffer
-        mbar_wait(bar(B_DV_DONE), (it - 1) & 1, wctx, ERR_SITE_BWD | 0x23);
-        tc_fence_after();
-      }
-      // P^T tile: row = key t, 128B-swizzled halves of 64 queries
 #pragma unroll
-      for (int c = 0; c < CW / 8; ++c) {
-        const int col = w * CW + c * 8;
-        const int half = col >> 6, chunk = (col & 63) >> 3;
-        st_shared_v4(sbase + C::OFF_P + half * C::KHALF + t * 128 + ((chunk ^ (t & 7)) << 4),
-                     pack_bf16x2(pv[c * 8], pv[c * 8 + 1]), pack_bf16x2(pv[c * 8 + 2], pv[c * 8 + 3]),
-                     pack_bf16x2(pv[c * 8 + 4], pv[c * 8 + 5]),
-                     pack_bf16x2(pv[c * 8 + 6], pv[c * 8 + 7]));
+      for (int c = 0; c < NCH; ++c) {  // 32 queries -> 16 packed columns, in this WG's S^T
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pv[c * 32 + 2 * e], pv[c * 32 + 2 * e + 1]);
+        tmem_st16(tS + c * 16, pk);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_P_FULL));
 
       // ---- dS^T = P^T o (dP^T - D)
       mbar_wait(bar(B_DP_FULL), it & 1, wctx, ERR_SITE_BWD | 0x24);
       tc_fence_after();
-      {
-        uint32_t u[NCH][32];
 #pragma unroll
-        for (int c = 0; c < NCH; ++c)
-          tmem_ld32(tmem + lane_off + C::TM_DP + w * CW + c * 32, u[c]);
-        tmem_wait_ld();
+      for (int c = 0; c < NCH; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tDP + c * 32, u);
+        tmem_wait_ld(u);
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) reg_fence32(u[c]);
-        tc_fence_before();
-        mbar_arrive(bar(B_DP_FREE));
-#pragma unroll
-        for (int c = 0; c < CW; ++c) pv[c] = pv[c] * (__uint_as_float(u[c >> 5][c & 31]) - dlt[c]);
+        for (int i = 0; i < 32; ++i)
+          pv[c * 32 + i] = pv[c * 32 + i] * (__uint_as_float(u[i]) - dlt[c * 32 + i]);
       }
+      tc_fence_before();
+      mbar_arrive(bar(B_DP_FREE));
       mbar_arrive(bar(B_Q_EMPTY + st));  // LSE2 and D of this stage are no longer read
       if (it > 0) {  // the previous dK / dQ MMAs have read the dS^T buffer
-        mbar_wait(bar(B_DQ_FULL), (it - 1) & 1, wctx, ERR_SITE_BWD | 0x25);
+        mbar_wait(bar(B_DS_FREE), (it - 1) & 1, wctx, ERR_SITE_BWD | 0x25);
         tc_fence_after();
       }
 #pragma unroll
@@ -401,16 +404,14 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
                      pack_bf16x2(pv[c * 8 + 6], pv[c * 8 + 7]));
       }
       fence_proxy_async_smem();
-      tc_fence_before();
       mbar_arrive(bar(B_DS_FULL));
-
-      if (it > 0) drain_dq(it - 1);
     }
-    mbar_wait(bar(B_DQ_FULL), (n_it - 1) & 1, wctx, ERR_SITE_BWD | 0x26);
-    tc_fence_after();
-    drain_dq(n_it - 1);
 
     // ---- epilogue: dK = scale * acc, dV = acc -> bf16 -> smem (K/V tiles are free) -> TMA
+    // the last dQ commit covers every MMA of the CTA
+    const int last = n_it - 1;
+    mbar_wait(bar(B_DQ_FULL + (last & 1)), (last >> 1) & 1, wctx, ERR_SITE_BWD | 0x26);
+    tc_fence_after();
     constexpr int EW = D / 2;  // d columns per warpgroup
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
@@ -459,10 +460,10 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
 template <int D>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                    const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                   const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
+                   const BwdParams& p, cudaStream_t stream) {
   using C = Bwd<D>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
-  static_assert(C::TM_DQ + (D == 128 ? C::BQ : D) <= 512, "TMEM budget");
+  static_assert(C::TM_DQ + 2 * C::DQC <= 512, "TMEM budget");
   cudaError_t e = cudaFuncSetAttribute(fattn_bwd_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
@@ -470,7 +471,7 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   const long long blocks = n_kb * p.BH;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   fattn_bwd_kernel<D><<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdk,
-                                                                          tdv, tdq, p);
+                                                                          tdv, p);
   return cudaGetLastError();
 }
 
@@ -478,10 +479,10 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
 
 cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
-                            const CUtensorMap& tdk, const CUtensorMap& tdv,
-                            const CUtensorMap& tdq_acc, const BwdParams& p, cudaStream_t stream) {
-  if (d == 128) return launch<128>(tq, tk, tv, tdo, tdk, tdv, tdq_acc, p, stream);
-  if (d == 64) return launch<64>(tq, tk, tv, tdo, tdk, tdv, tdq_acc, p, stream);
+                            const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdParams& p,
+                            cudaStream_t stream) {
+  if (d == 128) return launch<128>(tq, tk, tv, tdo, tdk, tdv, p, stream);
+  if (d == 64) return launch<64>(tq, tk, tv, tdo, tdk, tdv, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -11,8 +11,9 @@
 // Warp roles (320 threads):
 //   warps 0-3  softmax for Q_0, warps 4-7 softmax for Q_1: thread t owns query
 //              row t, which is TMEM lane t, so the row max and row sum need no
-//              shuffles.  They also rescale their O accumulator by alpha and
-//              run the epilogue O = o~ / l, LSE = m + ln l.
+//              shuffles.  They also rescale their O accumulator by alpha when
+//              the reference maximum moves, and run the epilogue O = o~ / l,
+//              LSE = m + ln l.
 //   warp 8     one thread issues every tcgen05.mma and commit.
 //   warp 9     one thread issues every TMA load.
 //
@@ -29,6 +30,8 @@ namespace fattn {
 namespace {
 
 constexpr float kLn2 = 0.6931471805599453f;
+// Largest exp2 argument the softmax lets through before it moves its reference.
+constexpr float kRescaleLog2 = 8.f;
 
 template <int D>
 struct Fwd {
@@ -255,18 +258,25 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
         ++n_full;
       }
 
-      float mx0 = m_run, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+      float mx[8];
 #pragma unroll
-      for (int k = 0; k < 128; k += 4) {
-        mx0 = fmaxf(mx0, sv[k]);
-        mx1 = fmaxf(mx1, sv[k + 1]);
-        mx2 = fmaxf(mx2, sv[k + 2]);
-        mx3 = fmaxf(mx3, sv[k + 3]);
-      }
-      const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      for (int i = 0; i < 8; ++i) mx[i] = i == 0 ? m_run : -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 128; k += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], sv[k + 2 * i], sv[k + 2 * i + 1]);
+      const float m_blk = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                fmaxf(mx[6], mx[7]));  // max(m_old, block max)
+      // The reference only moves when the block raises it by more than 2^8
+      // (in base 2); until then p = exp2(s - m) <= 2^8 and O, l stay in the
+      // old reference.  Any reference gives the same O and LSE (the shift
+      // invariance of softmax), and skipping small moves skips most rescales
+      // of O.  The first block always sets it (m_old = -inf).
+      const float m_new = (m_run == -INFINITY || (m_blk - m_run) * sl2 > kRescaleLog2) ? m_blk : m_run;
       const float msc = (m_new == -INFINITY) ? 0.f : m_new * sl2;
-      const float alpha = ex2(m_run * sl2 - msc);  // exp(m_old - m_new); 0 on the first block
       const bool rescale = m_new != m_run;
+      // alpha = exp(m_old - m_new): 0 on the first block, exactly 1 when the reference stays
+      const float alpha = rescale ? ex2(m_run * sl2 - msc) : 1.f;
       float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {  // 64 keys -> 32 packed bf16x2 TMEM columns

@@ -65,7 +65,7 @@ struct WaitCtx {
   unsigned int* err;              // global, may be null
 };
 
-static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
                                             uint32_t site) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -296,6 +296,13 @@ __device__ __forceinline__ float lg2(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 // Two fp32 -> packed bf16x2 (round to nearest even); lo goes to the low half.

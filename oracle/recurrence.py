@@ -11,7 +11,10 @@ normalizer" and the eight-score table of "Decoding flash attention".
 
 The model exists to pin the pages' worked examples and invariants (stability:
 every exp argument <= 0; exactness: block size and order do not change the
-result).  The ``pitfall`` switch plants, on purpose, each of the four mistakes
+result).  ``slack`` > 0 keeps the old reference m unless a block raises the
+maximum by more than ``slack``: the page's shift invariance ("for ANY constant
+m", section "Safe softmax: the max-subtraction we cannot give up") says the
+result is unchanged, and every exp argument stays <= slack instead of <= 0.  The ``pitfall`` switch plants, on purpose, each of the four mistakes
 listed under page 3's "Pitfalls in implementing the recurrence", so that tests
 can show the checks catch them:
 
@@ -30,7 +33,7 @@ def _axpy(alpha, x, y):
     return [alpha * a + b for a, b in zip(x, y)]
 
 
-def online_softmax_attention(scores, values, blocks, visible=None, pitfall=None):
+def online_softmax_attention(scores, values, blocks, visible=None, pitfall=None, slack=0.0):
     """Run the block-wise recurrence for one query.
 
     scores  -- list of raw scaled scores s_j (floats)
@@ -38,6 +41,8 @@ def online_softmax_attention(scores, values, blocks, visible=None, pitfall=None)
     blocks  -- list of lists of key indices, visited in the given order
     visible -- optional list of bools; False marks a masked key (causal or padding)
     pitfall -- None or one of PITFALLS
+    slack   -- 0 for the page's algorithm (m is the running max); > 0 moves m
+               only when the block maximum exceeds it by more than ``slack``
 
     Returns (o, m, l, trace).  trace is one dict per block with the block
     maximum, m_new, alpha, the p_j, l, o~ and every exp argument used.
@@ -55,6 +60,8 @@ def online_softmax_attention(scores, values, blocks, visible=None, pitfall=None)
         masked = [s if ok else -math.inf for s, ok in zip(raw, vis)]
         m_blk = max(raw) if pitfall == "mask_after_max" else max(masked)
         m_new = max(m, m_blk)
+        if slack > 0 and m != -math.inf and m_new - m <= slack:
+            m_new = m  # keep the old reference
         args = []
         if m_new == -math.inf:
             # nothing visible yet: exp(-inf - (-inf)) is undefined; the state stays empty

@@ -141,3 +141,35 @@ def test_each_pitfall_is_caught(pitfall):
     np.testing.assert_allclose(good, o_ref, rtol=1e-13)
     bad, _, _, _ = online_softmax_attention(case["scores"], values, blocks, case["visible"], pitfall)
     assert not np.allclose(bad, o_ref, rtol=1e-6, atol=1e-6, equal_nan=False), pitfall
+
+
+# ---------------------------------------------------------------- lazily moved reference
+
+@pytest.mark.parametrize("slack", [0.5, 2.0, 8 * math.log(2.0), 40.0])
+@pytest.mark.parametrize("size", [1, 4, 7, 200])
+def test_lazily_moved_reference_is_exact_and_bounded(slack, size):
+    """Keeping the old reference while the block max rises by at most ``slack``
+    gives the three-pass result (any reference works), and no exp argument
+    exceeds ``slack``.  The forward kernel uses slack = 8 ln 2 (2^8 in base 2)."""
+    scores, values = _random_case(500 + size, n=200, spread=12.0)
+    o_ref, lse_ref = _three_pass(scores, values)
+    o, m, l, trace = online_softmax_attention(scores, values, blocks_of(200, size), slack=slack)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-13)
+    assert abs(m + math.log(l) - lse_ref) < 1e-12
+    assert max(a for t in trace for a in t["exp_args"]) <= slack + 1e-12
+    assert all(0.0 < t["alpha"] <= 1.0 for t in trace[1:])
+    # the reference is never below the first block's max, never above the running max
+    seen = []
+    for i, t in enumerate(trace):
+        seen += scores[size * i: size * i + size]
+        assert t["m_new"] <= max(seen)
+        assert max(seen) - t["m_new"] <= slack
+
+
+def test_lazy_reference_skips_rescales():
+    scores, values = _random_case(600, n=512, spread=1.0)
+    _, _, _, exact = online_softmax_attention(scores, values, blocks_of(512, 16))
+    _, _, _, lazy = online_softmax_attention(scores, values, blocks_of(512, 16), slack=8 * math.log(2))
+    moves = lambda tr: sum(1 for t in tr[1:] if t["alpha"] != 1.0)
+    assert moves(lazy) < moves(exact)
+    assert moves(lazy) == 0  # N(0,1) scores never climb 5.5 above the first block's max

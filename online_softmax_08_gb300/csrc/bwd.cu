@@ -37,6 +37,7 @@
 // warpgroup owns key row t = TMEM lane t, warpgroup w owns half the query
 // columns), warps 8-11 drain dQ, warp 12 issues MMAs, warp 13 issues TMA loads
 // and stages LSE and D, warps 14-15 idle.
+#define FATTN_INLINE_WAIT_SLOW_PATH
 #include "common.cuh"
 #include "ptx.cuh"
 

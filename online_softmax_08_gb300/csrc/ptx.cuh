@@ -65,7 +65,15 @@ struct WaitCtx {
   unsigned int* err;              // global, may be null
 };
 
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
+// A translation unit may define FATTN_INLINE_WAIT_SLOW_PATH before including
+// this header to inline the timed polling loop at every wait (measured faster
+// for the backward kernel, slower for the forward kernel).
+#ifdef FATTN_INLINE_WAIT_SLOW_PATH
+#define FATTN_WAIT_SLOW_ATTR __forceinline__
+#else
+#define FATTN_WAIT_SLOW_ATTR __noinline__
+#endif
+static __device__ FATTN_WAIT_SLOW_ATTR bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
                                             uint32_t site) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {

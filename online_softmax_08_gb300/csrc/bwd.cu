@@ -35,8 +35,9 @@
 //
 // Warp roles (512 threads): warps 0-7 compute (two warpgroups; thread t of a
 // warpgroup owns key row t = TMEM lane t, warpgroup w owns half the query
-// columns), warps 8-11 drain dQ, warp 12 issues MMAs, warp 13 issues TMA loads
-// and stages LSE and D, warps 14-15 idle.
+// columns), warps 8-11 drain dQ, warp 12 issues MMAs (the whole warp runs the
+// loop, elect.sync picks the issuing lane), warp 13 issues TMA loads and
+// stages LSE and D, warps 14-15 idle.
 #define FATTN_INLINE_WAIT_SLOW_PATH
 #include "common.cuh"
 #include "ptx.cuh"
@@ -165,10 +166,14 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
       }
     }
     const float kLog2e = 1.4426950408889634f;
+    int issued = 0;
     for (int it = 0; it < n_it; ++it) {
       const int st = it % QST, use = it / QST;
       const int q0 = (i_start + it) * BQ;
-      if (use > 0) mbar_wait(bar(B_Q_EMPTY + st), (use - 1) & 1, wctx, ERR_SITE_BWD | 0x01);
+      // a stage is refilled only after its readers are done; when the CTA is
+      // aborting nothing more is issued (the decision is uniform over the warp)
+      bool ok = use == 0 || mbar_wait(bar(B_Q_EMPTY + st), (use - 1) & 1, wctx, ERR_SITE_BWD | 0x01);
+      if (!__all_sync(0xffffffffu, ok)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar(B_Q_FULL + st), 2 * C::TILE_Q);
         for (int h = 0; h < D / 64; ++h) {
@@ -187,16 +192,17 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
         stat[BQ + c] = ok ? p.delta[(size_t)bh * N + q] : 0.f;
       }
       mbar_arrive(bar(B_Q_FULL + st));
+      issued = it + 1;
     }
-    if (lane == 0) {
-      mbar_wait(bar(B_KV), 0, wctx, ERR_SITE_BWD | 0x02);
-      for (int it = max(0, n_it - QST); it < n_it; ++it)
-        mbar_wait(bar(B_Q_FULL + it % QST), (it / QST) & 1, wctx, ERR_SITE_BWD | 0x03);
+    if (lane == 0) {  // drain: at most one load per stage can still be landing
+      mbar_drain(bar(B_KV), 0, wctx, ERR_SITE_BWD | 0x02);
+      for (int it = max(0, issued - QST); it < issued; ++it)
+        mbar_drain(bar(B_Q_FULL + it % QST), (it / QST) & 1, wctx, ERR_SITE_BWD | 0x03);
     }
     __syncwarp();
   } else if (warp == 12) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer (whole warp)
+    {
       const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sDS = sbase + C::OFF_DS;
       // D[128 x BQ] = X[128 keys x D] * Y[BQ x D]^T, both K-major
       auto mma_xyT = [&](uint32_t d_col, uint32_t x, uint32_t y) {
@@ -204,7 +210,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t xo = (kk >> 2) * C::KHALF + (kk & 3) * 32;
           const uint32_t yo = (kk >> 2) * C::QHALF + (kk & 3) * 32;
-          mma_bf16_ss(tmem + d_col, sdesc_sw128(x + xo, 16, 1024), sdesc_sw128(y + yo, 16, 1024),
+          mma_bf16_ss_w(tmem + d_col, sdesc_sw128(x + xo, 16, 1024), sdesc_sw128(y + yo, 16, 1024),
                       C::IDESC_S, kk > 0);
         }
       };
@@ -212,7 +218,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
       auto mma_dv = [&](uint32_t sdo, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_bf16_ts(tmem + C::TM_DV, tmem + C::p_col(kk),
+          mma_bf16_ts_w(tmem + C::TM_DV, tmem + C::p_col(kk),
                       sdesc_sw128(sdo + kk * 16 * 128, C::QHALF, 1024), C::IDESC_ACC,
                       (acc || kk > 0));
       };
@@ -221,7 +227,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t ao = (kk >> 2) * C::KHALF + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::TM_DK, sdesc_sw128(sDS + ao, 16, 1024),
+          mma_bf16_ss_w(tmem + C::TM_DK, sdesc_sw128(sDS + ao, 16, 1024),
                       sdesc_sw128(sq + kk * 16 * 128, C::QHALF, 1024), C::IDESC_ACC,
                       (acc || kk > 0));
         }
@@ -232,57 +238,64 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
         for (int kk = 0; kk < C::BK / 16; ++kk) {
           const uint32_t o = kk * 16 * 128;
           if (D == 128)  // dQ^T[d x BQ] = K^T[d x keys] * dS^T[keys x BQ]
-            mma_bf16_ss(tmem + d_col, sdesc_sw128(sK + o, C::KHALF, 1024),
+            mma_bf16_ss_w(tmem + d_col, sdesc_sw128(sK + o, C::KHALF, 1024),
                         sdesc_sw128(sDS + o, C::KHALF, 1024), C::IDESC_DQ, kk > 0);
           else  // dQ[BQ x d] = dS[BQ x keys] * K[keys x d]
-            mma_bf16_ss(tmem + d_col, sdesc_sw128(sDS + o, C::KHALF, 1024),
+            mma_bf16_ss_w(tmem + d_col, sdesc_sw128(sDS + o, C::KHALF, 1024),
                         sdesc_sw128(sK + o, C::KHALF, 1024), C::IDESC_DQ, kk > 0);
         }
       };
       auto q_wait = [&](int it) {
-        mbar_wait(bar(B_Q_FULL + it % QST), (it / QST) & 1, wctx, ERR_SITE_BWD | 0x11);
+        return __all_sync(0xffffffffu,
+                          mbar_wait(bar(B_Q_FULL + it % QST), (it / QST) & 1, wctx, ERR_SITE_BWD | 0x11));
       };
       auto sQ = [&](int it) { return sbase + C::OFF_Q + (it % QST) * C::TILE_Q; };
       auto sDO = [&](int it) { return sbase + C::OFF_DO + (it % QST) * C::TILE_Q; };
 
-      mbar_wait(bar(B_KV), 0, wctx, ERR_SITE_BWD | 0x12);
-      q_wait(0);
-      tc_fence_after();
-      mma_xyT(C::TM_S, sK, sQ(0));
-      mma_commit(bar(B_S_FULL));
-      mma_xyT(C::TM_DP, sV, sDO(0));
-      mma_commit(bar(B_DP_FULL));
-      for (int it = 0; it < n_it; ++it) {
+      // any failed wait means the CTA is aborting: issue nothing more
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_KV), 0, wctx, ERR_SITE_BWD | 0x12));
+      ok = ok && q_wait(0);
+      if (ok) {
+        tc_fence_after();
+        mma_xyT(C::TM_S, sK, sQ(0));
+        mma_commit_w(bar(B_S_FULL));
+        mma_xyT(C::TM_DP, sV, sDO(0));
+        mma_commit_w(bar(B_DP_FULL));
+      }
+      for (int it = 0; ok && it < n_it; ++it) {
         const bool next = it + 1 < n_it;
-        mbar_wait(bar(B_P_FULL), it & 1, wctx, ERR_SITE_BWD | 0x13);
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(B_P_FULL), it & 1, wctx, ERR_SITE_BWD | 0x13)))) break;
         tc_fence_after();
         mma_dv(sDO(it), it > 0);
         if (next) {  // overwrites S^T / P^T: after the dV above in pipe order
-          q_wait(it + 1);
+          if (!(ok = q_wait(it + 1))) break;
           mma_xyT(C::TM_S, sK, sQ(it + 1));
-          mma_commit(bar(B_S_FULL));
+          mma_commit_w(bar(B_S_FULL));
         }
-        mbar_wait(bar(B_DS_FULL), it & 1, wctx, ERR_SITE_BWD | 0x15);
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DS_FULL), it & 1, wctx, ERR_SITE_BWD | 0x15)))) break;
         tc_fence_after();
         mma_dk(sQ(it), it > 0);
         if (next) {
-          mbar_wait(bar(B_DP_FREE), it & 1, wctx, ERR_SITE_BWD | 0x16);
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DP_FREE), it & 1, wctx, ERR_SITE_BWD | 0x16)))) break;
           tc_fence_after();
           mma_xyT(C::TM_DP, sV, sDO(it + 1));
-          mma_commit(bar(B_DP_FULL));
+          mma_commit_w(bar(B_DP_FULL));
         }
         const int b = it & 1;
         if (it >= 2) {
-          mbar_wait(bar(B_DQ_FREE + b), ((it - 2) >> 1) & 1, wctx, ERR_SITE_BWD | 0x17);
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DQ_FREE + b), ((it - 2) >> 1) & 1,
+                                                        wctx, ERR_SITE_BWD | 0x17))))
+            break;
           tc_fence_after();
         }
         mma_dq(C::TM_DQ + b * C::DQC);
-        mma_commit(bar(B_DQ_FULL + b));
-        mma_commit(bar(B_DS_FREE));
-        mma_commit(bar(B_Q_EMPTY + it % QST));
+        mma_commit_w(bar(B_DQ_FULL + b));
+        mma_commit_w(bar(B_DS_FREE));
+        mma_commit_w(bar(B_Q_EMPTY + it % QST));
       }
-      mma_commit(bar(B_MMA_DONE));
-      mbar_wait(bar(B_MMA_DONE), 0, wctx, ERR_SITE_BWD | 0x18);
+      // drain: every MMA issued by this thread has finished before TMEM is freed
+      mma_commit_w(bar(B_MMA_DONE));
+      mbar_drain(bar(B_MMA_DONE), 0, wctx, ERR_SITE_BWD | 0x18);
     }
     __syncwarp();
   } else if (warp >= 8 && warp < 12) {

@@ -14,7 +14,9 @@
 //              shuffles.  They also rescale their O accumulator by alpha when
 //              the reference maximum moves, and run the epilogue O = o~ / l,
 //              LSE = m + ln l.
-//   warp 8     one thread issues every tcgen05.mma and commit.
+//   warp 8     issues every tcgen05.mma and commit: the whole warp runs the
+//              loop (so descriptor arithmetic stays warp-uniform) and
+//              elect.sync picks the one lane that issues.
 //   warp 9     one thread issues every TMA load.
 //
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 after it.
@@ -140,26 +142,31 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
             tma_load_3d(sbase + C::OFF_Q + s * C::TILE + h * C::HALF, &tm_q, bar(B_Q), h * 64,
                         r0[s], bh);
       const int n_loads = 2 * n_max;
+      int issued = 0;
       for (int i = 0; i < n_loads; ++i) {
         const int slot = i % ST, use = i / ST;
-        if (use > 0) mbar_wait(kv_empty0 + 8u * slot, (use - 1) & 1, wctx, ERR_SITE_FWD | 0x01);
+        // a slot is refilled only after the MMAs that read it completed; when
+        // the CTA is aborting nothing more is issued
+        if (use > 0 && !mbar_wait(kv_empty0 + 8u * slot, (use - 1) & 1, wctx, ERR_SITE_FWD | 0x01))
+          break;
         const uint32_t dst = sbase + C::OFF_KV + slot * C::TILE;
         const CUtensorMap* m = (i & 1) ? &tm_v : &tm_k;
         mbar_arrive_expect_tx(kv_full0 + 8u * slot, C::TILE);
         for (int h = 0; h < D / 64; ++h)
           tma_load_3d(dst + h * C::HALF, m, kv_full0 + 8u * slot, h * 64, (i >> 1) * C::BN, bh);
+        issued = i + 1;
       }
-      // make sure no load is still landing when the CTA leaves
-      for (int i = max(0, n_loads - ST); i < n_loads; ++i)
-        mbar_wait(kv_full0 + 8u * (i % ST), (i / ST) & 1, wctx, ERR_SITE_FWD | 0x02);
-      mbar_wait(bar(B_Q), 0, wctx, ERR_SITE_FWD | 0x03);
+      // drain: at most one load per slot can still be landing, the latest one
+      for (int i = max(0, issued - ST); i < issued; ++i)
+        mbar_drain(kv_full0 + 8u * (i % ST), (i / ST) & 1, wctx, ERR_SITE_FWD | 0x02);
+      mbar_drain(bar(B_Q), 0, wctx, ERR_SITE_FWD | 0x03);
     }
     __syncwarp();
   } else if (warp == 8) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer (whole warp)
+    {
       auto kv_wait = [&](int i) {
-        mbar_wait(kv_full0 + 8u * (i % ST), (i / ST) & 1, wctx, ERR_SITE_FWD | 0x11);
+        return __all_sync(0xffffffffu, mbar_wait(kv_full0 + 8u * (i % ST), (i / ST) & 1, wctx, ERR_SITE_FWD | 0x11));
       };
       auto issue_s = [&](int s, int j) {  // S_s = Q_s K_j^T
         const uint32_t a = sbase + C::OFF_Q + s * C::TILE;
@@ -167,49 +174,56 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::HALF + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::TM_S + s * 128, sdesc_sw128(a + off, 16, 1024),
+          mma_bf16_ss_w(tmem + C::TM_S + s * 128, sdesc_sw128(a + off, 16, 1024),
                       sdesc_sw128(b + off, 16, 1024), C::IDESC_S, kk > 0);
         }
-        mma_commit(bar(B_S_FULL + s));
+        mma_commit_w(bar(B_S_FULL + s));
       };
       auto issue_pv = [&](int s, int j) {  // O_s += P_s V_j, P_s from TMEM
         const uint32_t b = sbase + C::OFF_KV + ((2 * j + 1) % ST) * C::TILE;
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)  // 16 keys = 8 packed TMEM columns per step
-          mma_bf16_ts(tmem + C::TM_O + s * D, tmem + C::TM_S + s * 128 + kk * 8,
+          mma_bf16_ts_w(tmem + C::TM_O + s * D, tmem + C::TM_S + s * 128 + kk * 8,
                       sdesc_sw128(b + kk * 16 * 128, C::HALF, 1024), C::IDESC_PV,
                       (j > 0 || kk > 0));
-        mma_commit(bar(B_PV_DONE + s));
+        mma_commit_w(bar(B_PV_DONE + s));
       };
-      mbar_wait(bar(B_Q), 0, wctx, ERR_SITE_FWD | 0x12);
-      if (n_max > 0) {
-        kv_wait(0);
-        tc_fence_after();
-        if (nt0 > 0) issue_s(0, 0);
-        if (nt1 > 0) issue_s(1, 0);
-        mma_commit(kv_empty0 + 8u * 0);
+      // any failed wait means the CTA is aborting: issue nothing more
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q), 0, wctx, ERR_SITE_FWD | 0x12));
+      if (ok && n_max > 0) {
+        ok = kv_wait(0);
+        if (ok) {
+          tc_fence_after();
+          if (nt0 > 0) issue_s(0, 0);
+          if (nt1 > 0) issue_s(1, 0);
+          mma_commit_w(kv_empty0 + 8u * 0);
+        }
       }
-      for (int j = 0; j < n_max; ++j) {
+      for (int j = 0; ok && j < n_max; ++j) {
         const bool next = j + 1 < n_max;
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           const int nts = s ? nt1 : nt0;
-          if (j < nts) {
-            kv_wait(2 * j + 1);
-            mbar_wait(bar(B_P_FULL + s), j & 1, wctx, ERR_SITE_FWD | 0x14);
-            tc_fence_after();
-            issue_pv(s, j);
+          if (ok && j < nts) {
+            ok = kv_wait(2 * j + 1) &&
+                 __all_sync(0xffffffffu, mbar_wait(bar(B_P_FULL + s), j & 1, wctx, ERR_SITE_FWD | 0x14));
+            if (ok) {
+              tc_fence_after();
+              issue_pv(s, j);
+            }
           }
-          if (j + 1 < nts) {  // after the PV above: S_s is overwritten in pipe order
-            kv_wait(2 * (j + 1));
-            issue_s(s, j + 1);
+          if (ok && j + 1 < nts) {  // after the PV above: S_s is overwritten in pipe order
+            ok = kv_wait(2 * (j + 1));
+            if (ok) issue_s(s, j + 1);
           }
         }
-        if (next) mma_commit(kv_empty0 + 8u * ((2 * (j + 1)) % ST));
-        mma_commit(kv_empty0 + 8u * ((2 * j + 1) % ST));
+        if (!ok) break;
+        if (next) mma_commit_w(kv_empty0 + 8u * ((2 * (j + 1)) % ST));
+        mma_commit_w(kv_empty0 + 8u * ((2 * j + 1) % ST));
       }
-      mma_commit(bar(B_MMA_DONE));
-      mbar_wait(bar(B_MMA_DONE), 0, wctx, ERR_SITE_FWD | 0x17);
+      // drain: every MMA issued by this thread has finished before TMEM is freed
+      mma_commit_w(bar(B_MMA_DONE));
+      mbar_drain(bar(B_MMA_DONE), 0, wctx, ERR_SITE_FWD | 0x17);
     }
     __syncwarp();
   } else {

@@ -1,18 +1,20 @@
 // ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarriers, TMA, tcgen05/TMEM.
 //
-// Every wait on an mbarrier is bounded: after FATTN_WAIT_TIMEOUT_NS of
-// %globaltimer the waiting thread records an error code in a device word,
-// raises the CTA's abort flag and returns false, so a kernel never spins
-// forever.  Once the abort flag is up, every later wait of the CTA gives up
-// at once and the kernel runs to its end without touching memory it does
-// not own.
+// Every wait on an mbarrier is bounded: after FATTN_WAIT_TIMEOUT_CYCLES SM
+// clock cycles (%clock64: per-SM, monotonic, never adjusted by the driver) the
+// waiting thread records an error code in a device word, raises the CTA's
+// abort flag and returns false, so a kernel never spins forever.  Once the
+// abort flag is up, the kernels stop issuing new loads and MMAs, and each role
+// still drains its own asynchronous work in flight (mbar_drain, which waits
+// even when the CTA is aborting, again with a limit) before TMEM is freed and
+// the CTA exits.
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#ifndef FATTN_WAIT_TIMEOUT_NS
-#define FATTN_WAIT_TIMEOUT_NS 2000000000ull
+#ifndef FATTN_WAIT_TIMEOUT_CYCLES
+#define FATTN_WAIT_TIMEOUT_CYCLES 4000000000ll  // about 2 s at 2 GHz
 #endif
 
 namespace fattn {
@@ -21,9 +23,9 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+__device__ __forceinline__ long long clock_cycles() {
+  long long t;
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));
   return t;
 }
 
@@ -73,15 +75,16 @@ struct WaitCtx {
 #else
 #define FATTN_WAIT_SLOW_ATTR __noinline__
 #endif
-static __device__ FATTN_WAIT_SLOW_ATTR bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
-                                            uint32_t site) {
-  const uint64_t t0 = globaltimer_ns();
+static __device__ FATTN_WAIT_SLOW_ATTR bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                          const WaitCtx& ctx, uint32_t site,
+                                                          bool drain) {
+  const long long t0 = clock_cycles();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 256; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (*ctx.abort_flag) return false;
-    if (globaltimer_ns() - t0 > FATTN_WAIT_TIMEOUT_NS) {
+    if (!drain && *ctx.abort_flag) return false;
+    if (clock_cycles() - t0 > FATTN_WAIT_TIMEOUT_CYCLES) {  // signed: immune to wrap
       *ctx.abort_flag = 1u;
       if (ctx.err) atomicCAS(ctx.err, 0u, site);
       return false;
@@ -89,12 +92,23 @@ static __device__ FATTN_WAIT_SLOW_ATTR bool mbar_wait_slow(uint32_t bar, uint32_
   }
 }
 
-// Wait for completion of the phase with the given parity; false on timeout/abort.
+// Wait for completion of the phase with the given parity; false on timeout,
+// or at once when the CTA is already aborting.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
                                           uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, ctx, site);
+  return mbar_wait_slow(bar, parity, ctx, site, false);
 }
+
+// Wait for the CTA's own asynchronous work (TMA copies, MMAs) to finish, even
+// when the CTA is aborting; false only on timeout.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
+                                           uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, ctx, site, true);
+}
+
+__device__ __forceinline__ bool aborting(const WaitCtx& ctx) { return *ctx.abort_flag != 0u; }
 
 // ------------------------------------------------------------------ proxies / named barriers
 
@@ -192,6 +206,36 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Warp-wide variants: every lane of a converged warp executes them, one lane
+// (elect.sync: the lowest) issues the operation.
+__device__ __forceinline__ void mma_bf16_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_w(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
       : "memory");
 }
 

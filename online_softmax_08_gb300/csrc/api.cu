@@ -155,10 +155,14 @@ extern "C" int fattn_bwd_ex(const void* q, const void* k, const void* v, const v
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int bq = 0, bk = 0;
   fattn_tile_sizes(d, 1, &bq, &bk);
-  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
   if (!make_bf16_map(&tq, q, d, N, BH, bq) || !make_bf16_map(&tdo, dout, d, N, BH, bq) ||
       !make_bf16_map(&tk, k, d, N, BH, bk) || !make_bf16_map(&tv, v, d, N, BH, bk) ||
       !make_bf16_map(&tdk, dk, d, N, BH, bk) || !make_bf16_map(&tdv, dv, d, N, BH, bk))
+    return FATTN_ERR_CUDA;
+  // dQ accumulator: fp32, add-reduced 32 query rows at a time
+  if (!make_map(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, BH, d, 32,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
     return FATTN_ERR_CUDA;
   auto mark = [&](int i) {
     return !phase_events ||
@@ -178,7 +182,7 @@ extern "C" int fattn_bwd_ex(const void* q, const void* k, const void* v, const v
   p.delta = delta;
   p.dq_acc = dq_acc;
   p.err = dev->err;
-  cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, tdk, tdv, p, s);
+  cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, tdk, tdv, tdq, p, s);
   if (e == cudaErrorNotSupported) return FATTN_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return FATTN_ERR_CUDA;
   if (!mark(2)) return FATTN_ERR_CUDA;
@@ -199,7 +203,7 @@ extern "C" int fattn_tile_sizes(int d, int pass, int* block_q, int* block_k) {
   if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
   if (pass != 0 && pass != 1) return FATTN_ERR_INVALID_ARG;
   int bq = 128, bk = 128;
-  if (pass == 1) bq = (d == 128) ? 64 : 128;
+  if (pass == 1) bq = 64;
   if (block_q) *block_q = bq;
   if (block_k) *block_k = bk;
   return FATTN_OK;

@@ -43,8 +43,8 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* delta,
                                   long long rows, int d, cudaStream_t stream);
 cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
-                            const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdParams& p,
-                            cudaStream_t stream);
+                            const CUtensorMap& tdk, const CUtensorMap& tdv,
+                            const CUtensorMap& tdq_acc, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_convert(const float* dq_acc, void* dq, long long n, float scale,
                                cudaStream_t stream);
 

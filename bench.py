@@ -45,6 +45,23 @@ def flops(B, H, N, d, causal):
     return f, 2.5 * f
 
 
+def measured_traffic(kernel):
+    """DRAM bytes per launch of ``kernel`` from the committed ncu capture, or None
+    when the kernel's sources changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic_b1h32_n8192_d128_causal.json")
+    try:
+        with open(path) as f:
+            entry = json.load(f)["kernels"][kernel]
+        m = hashlib.sha256()
+        for name in entry["sources"]:
+            with open(os.path.join(ROOT, "online_softmax_08_gb300", "csrc", name), "rb") as f:
+                m.update(f.read())
+        return entry["bytes"] if m.hexdigest() == entry["sha256"] else None
+    except Exception:
+        return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -307,10 +324,15 @@ def run_gpu(args):
     fwd_bytes = 4 * rows * d * 2 + rows * 4
     roof = {"kernel": "fattn_bwd_kernel<%d>" % d, "bound": "tensor", "achieved": main_tf,
             "peak": peak_tf, "unit": "TFLOP/s", "frac": main_tf / peak_tf,
-            "peak_source": peak_src + " (bf16 burst)", "traffic": None}
+            "peak_source": peak_src + " (bf16 burst)",
+            "traffic": measured_traffic("fattn_bwd_kernel<%d>" % d) if args.workload == HEADLINE
+            else None,
+            "algorithmic_bytes": 8 * rows * d * 2 + 2 * rows * 4}
     roof_fwd = {"kernel": "fattn_fwd_kernel<%d>" % d, "bound": "tensor", "achieved": fwd_tf,
                 "peak": peak_tf, "unit": "TFLOP/s", "frac": fwd_tf / peak_tf,
-                "peak_source": peak_src + " (bf16 burst)", "traffic": None,
+                "peak_source": peak_src + " (bf16 burst)",
+                "traffic": measured_traffic("fattn_fwd_kernel<%d>" % d) if args.workload == HEADLINE
+                else None,
                 "algorithmic_bytes": fwd_bytes}
 
     # end to end through the C-ABI with host buffers: pinned H2D of Q, K, V, dO,

@@ -160,8 +160,8 @@ extern "C" int fattn_bwd_ex(const void* q, const void* k, const void* v, const v
       !make_bf16_map(&tk, k, d, N, BH, bk) || !make_bf16_map(&tv, v, d, N, BH, bk) ||
       !make_bf16_map(&tdk, dk, d, N, BH, bk) || !make_bf16_map(&tdv, dv, d, N, BH, bk))
     return FATTN_ERR_CUDA;
-  // dQ accumulator: fp32, add-reduced 32 query rows at a time
-  if (!make_map(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, BH, d, 32,
+  // dQ accumulator: fp32, add-reduced 16 query rows at a time
+  if (!make_map(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, BH, d, 16,
                 CU_TENSOR_MAP_SWIZZLE_NONE))
     return FATTN_ERR_CUDA;
   auto mark = [&](int i) {
@@ -202,8 +202,7 @@ extern "C" int fattn_bwd(const void* q, const void* k, const void* v, const void
 extern "C" int fattn_tile_sizes(int d, int pass, int* block_q, int* block_k) {
   if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
   if (pass != 0 && pass != 1) return FATTN_ERR_INVALID_ARG;
-  int bq = 128, bk = 128;
-  if (pass == 1) bq = 64;
+  const int bq = 128, bk = 128;  // both passes, both head sizes
   if (block_q) *block_q = bq;
   if (block_k) *block_k = bk;
   return FATTN_OK;

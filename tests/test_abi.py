@@ -43,8 +43,8 @@ def test_status_strings(lib):
 def test_tile_sizes(lib):
     assert fattn.fattn_tile_sizes(128, 0) == (128, 128)
     assert fattn.fattn_tile_sizes(64, 0) == (128, 128)
-    assert fattn.fattn_tile_sizes(128, 1) == (64, 128)
-    assert fattn.fattn_tile_sizes(64, 1) == (64, 128)
+    assert fattn.fattn_tile_sizes(128, 1) == (128, 128)
+    assert fattn.fattn_tile_sizes(64, 1) == (128, 128)
     with pytest.raises(fattn.FattnError):
         fattn.fattn_tile_sizes(96, 0)
 

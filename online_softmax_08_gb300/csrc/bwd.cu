@@ -25,11 +25,13 @@
 // is overwritten in place by the bf16 P^T, and a region Y that holds dP^T until
 // dS is formed and then dQ^T.  The MMA warp issues, per step i,
 //
-//   dV(i)  dP(i) -> Y  S(i+1) -> X  dK(i)  dQ(i) -> Y
+//   dP(i) -> Y  dV(i)  S(i+1) -> X  dK(i)  dQ(i) -> Y
 //
-// so the softmax of step i+1 runs while dK(i) and dQ(i) execute, and dS of
-// step i while S(i+1) executes.  The dS warpgroup copies P^T(i) into registers
-// as soon as it is formed, which frees X for S(i+1).  The dQ^T partial of each
+// dP(i) does not wait for P(i), so dS(i) starts as soon as it lands; dV(i) and
+// S(i+1) execute while dS(i) is formed, and P(i+1) is formed while dK(i),
+// dQ(i) and the next dP execute.  Each compute warpgroup keeps the bf16 P^T
+// of its 64 queries in registers from P to dS, so X can take S(i+1) right
+// after dV(i).  The dQ^T partial of each
 // step is read out of TMEM by a drain warpgroup (freeing Y for dP(i+1)) and
 // added into an fp32 accumulator with bulk tensor reduces of 16 query rows,
 // staged through two shared-memory buffers so that filling one overlaps the
@@ -37,11 +39,12 @@
 // buffer).  The alternative, a second pass parallel over query blocks, would
 // recompute S and dP (seven matmuls per tile instead of five).
 //
-// Warp roles (512 threads): warps 0-3 form P, warps 4-7 form dS (thread t of a
-// warpgroup owns key row t = TMEM lane t), warps 8-11 drain dQ, warp 12 issues
-// MMAs (the whole warp runs the loop, elect.sync picks the issuing lane), warp
-// 13 issues TMA loads and stages LSE and D, warps 14-15 idle.  Registers move
-// from the last warpgroup to the dS and drain warpgroups (setmaxnreg).
+// Warp roles (512 threads): warps 0-7 form P and dS, warpgroup w for queries
+// [64w, 64w + 64) of each step (thread t of a warpgroup owns key row t = TMEM
+// lane t), warps 8-11 drain dQ, warp 12 issues MMAs (the whole warp runs the
+// loop, elect.sync picks the issuing lane), warp 13 issues TMA loads and stages
+// LSE and D, warps 14-15 idle.  Registers move from the last warpgroup to the
+// drain warpgroup (setmaxnreg).
 #define FATTN_INLINE_WAIT_SLOW_PATH
 #include "common.cuh"
 #include "ptx.cuh"
@@ -62,7 +65,7 @@ struct Bwd {
   static constexpr int OFF_Q = OFF_V + TILE;                   // [QST]
   static constexpr int OFF_DO = OFF_Q + QST * TILE;            // [OST]
   static constexpr int OFF_DS = OFF_DO + OST * TILE;           // dS^T [128 keys][128 q] bf16
-  static constexpr int OFF_STAT = OFF_DS + 2 * HALF;           // [QST] x {lse2[BQ], delta[BQ]}
+  static constexpr int OFF_STAT = OFF_DS + 2 * HALF;           // [QST] x {-lse2[BQ], delta[BQ]}
   static constexpr int OFF_DQ = OFF_STAT + QST * 2 * BQ * 4;  // fp32 staging [2][16 q][D]
   static constexpr int OFF_BAR = OFF_DQ + 2 * 16 * D * 4;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
@@ -87,7 +90,7 @@ struct Bwd {
 // have consumed the current one (the MMA warp's issue order chains them).
 enum {
   B_KV = 0,
-  B_S_FULL = 1,     // MMA -> P warpgroup: S^T in X
+  B_S_FULL = 1,     // MMA -> compute warps: S^T in X
   B_P_FULL = 2,     // compute warps -> MMA: P^T (bf16) in X, S^T read
   B_DP_FULL = 4,    // MMA -> compute warps: dP^T in Y
   B_DS_FULL = 5,    // compute warps -> MMA: dS^T in shared memory, dP^T read
@@ -102,6 +105,34 @@ enum {
   B_COUNT = 20,
 };
 static_assert(Bwd<128>::QST <= 3 && Bwd<64>::QST <= 3 && Bwd<64>::OST <= 2, "barrier slots");
+
+// Two-lane fp32 arithmetic (one instruction for a pair of queries; each lane
+// rounds exactly as the scalar instruction would).
+// r = a * b + c with b shared by both lanes
+__device__ __forceinline__ void fma_x2(float a0, float a1, float b, float c0, float c1, float& r0,
+                                       float& r1) {
+  asm("{\n\t.reg .b64 a, b, c, r;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %4};\n\t"
+      "mov.b64 c, {%5, %6};\n\t"
+      "fma.rn.f32x2 r, a, b, c;\n\t"
+      "mov.b64 {%0, %1}, r;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c0), "f"(c1));
+}
+// r = p * (x - y)
+__device__ __forceinline__ void mul_sub_x2(float p0, float p1, float x0, float x1, float y0,
+                                           float y1, float& r0, float& r1) {
+  asm("{\n\t.reg .b64 p, x, y, r;\n\t"
+      "mov.b64 p, {%2, %3};\n\t"
+      "mov.b64 x, {%4, %5};\n\t"
+      "mov.b64 y, {%6, %7};\n\t"
+      "sub.rn.f32x2 x, x, y;\n\t"
+      "mul.rn.f32x2 r, p, x;\n\t"
+      "mov.b64 {%0, %1}, r;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(p0), "f"(p1), "f"(x0), "f"(x1), "f"(y0), "f"(y1));
+}
 
 template <int N>
 __device__ __forceinline__ void regs_inc() {
@@ -188,8 +219,8 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
       }
       const float kLog2e = 1.4426950408889634f;
       int q_issued = 0, o_issued = 0;
-      // Q(i) is released by dK(i), dO(i) by dP(i); in the MMA order dP(i) precedes
-      // dK(i) precedes dP(i + 1), so loading Q(i), dO(i) alternately never waits
+      // Q(i) is released by dK(i), dO(i) by dV(i); in the MMA order dV(i) precedes
+      // dK(i) precedes dV(i + 1), so loading Q(i), dO(i) alternately never waits
       // on a later release before an earlier one.
       for (int it = 0; it < n_it; ++it) {
         const int q0 = (i_start + it) * BQ;
@@ -210,8 +241,8 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
 #pragma unroll
           for (int j = 0; j < BQ / 32; ++j) {
             const int q = q0 + lane + 32 * j;
-            // a query past N gets LSE = +inf, so its P column is exactly zero
-            l[j] = q < N ? p.lse[(size_t)bh * N + q] * kLog2e : INFINITY;
+            // -LSE2; a query past N gets -inf, so its P column is exactly zero
+            l[j] = q < N ? -p.lse[(size_t)bh * N + q] * kLog2e : -INFINITY;
             dl[j] = q < N ? p.delta[(size_t)bh * N + q] : 0.f;
           }
 #pragma unroll
@@ -298,18 +329,18 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
       }
       for (int it = 0; ok && it < n_it; ++it) {
         const bool next = it + 1 < n_it;
-        // dV(i): P^T from X, dO(i)
-        if (!(ok = wait_all(B_P_FULL, it, 0x13) &&
-                   wait_all(B_O_FULL + it % OST, it / OST, 0x14)))
-          break;
-        tc_fence_after();
-        mma_dv(sDO(it), it > 0);
-        // dP(i) into Y once the drain has read dQ(i - 1)
+        // dP(i) into Y once the drain has read dQ(i - 1): it does not wait for P(i),
+        // so dS(i) can start as soon as it lands
+        if (!(ok = wait_all(B_O_FULL + it % OST, it / OST, 0x14))) break;
         if (it > 0 && !(ok = wait_all(B_DQ_FREE, it - 1, 0x17))) break;
         tc_fence_after();
         mma_xyT(C::TM_Y, sV, sDO(it));
         mma_commit_w(bar(B_DP_FULL));
-        mma_commit_w(bar(B_O_EMPTY + it % OST));  // dP is the last reader of dO(i)
+        // dV(i): P^T from X, dO(i)
+        if (!(ok = wait_all(B_P_FULL, it, 0x13))) break;
+        tc_fence_after();
+        mma_dv(sDO(it), it > 0);
+        mma_commit_w(bar(B_O_EMPTY + it % OST));  // dV is the last reader of dO(i)
         // S(i + 1) into X: dV(i), earlier in the pipe, was the last reader of P^T(i)
         if (next) {
           if (!(ok = wait_all(B_Q_FULL + (it + 1) % QST, (it + 1) / QST, 0x11))) break;
@@ -396,7 +427,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
       const int st = it % QST;
       const int q0 = (i_start + it) * BQ;
       mbar_wait(bar(B_Q_FULL + st), (it / QST) & 1, wctx, ERR_SITE_BWD | 0x21);
-      const float4* lse2 =
+      const float4* nlse2 =
           reinterpret_cast<const float4*>(smem + C::OFF_STAT + st * 2 * BQ * 4) + 16 * w;
       // key kr sees query q iff kr < N and (not causal or kr <= q); queries
       // past N already have LSE2 = +inf.  Only blocks that cross the diagonal
@@ -419,11 +450,13 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
         float pv[32];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          const float4 l4 = lse2[(c * 32 + i) / 4];
-          pv[i] = ex2(fmaf(__uint_as_float(u[c][i]), sl2, -l4.x));
-          pv[i + 1] = ex2(fmaf(__uint_as_float(u[c][i + 1]), sl2, -l4.y));
-          pv[i + 2] = ex2(fmaf(__uint_as_float(u[c][i + 2]), sl2, -l4.z));
-          pv[i + 3] = ex2(fmaf(__uint_as_float(u[c][i + 3]), sl2, -l4.w));
+          const float4 l4 = nlse2[(c * 32 + i) / 4];
+          fma_x2(__uint_as_float(u[c][i]), __uint_as_float(u[c][i + 1]), sl2, l4.x, l4.y, pv[i],
+                 pv[i + 1]);
+          fma_x2(__uint_as_float(u[c][i + 2]), __uint_as_float(u[c][i + 3]), sl2, l4.z, l4.w,
+                 pv[i + 2], pv[i + 3]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) pv[i + j] = ex2(pv[i + j]);
         }
         if (need_mask) {
 #pragma unroll
@@ -462,10 +495,12 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
         for (int i = 0; i < 32; i += 4) {
           const uint32_t p01 = pk[c * 16 + i / 2], p23 = pk[c * 16 + i / 2 + 1];
           const float4 d4 = dlt[(c * 32 + i) / 4];
-          ds[i] = __uint_as_float(p01 << 16) * (__uint_as_float(u[c][i]) - d4.x);
-          ds[i + 1] = __uint_as_float(p01 & 0xffff0000u) * (__uint_as_float(u[c][i + 1]) - d4.y);
-          ds[i + 2] = __uint_as_float(p23 << 16) * (__uint_as_float(u[c][i + 2]) - d4.z);
-          ds[i + 3] = __uint_as_float(p23 & 0xffff0000u) * (__uint_as_float(u[c][i + 3]) - d4.w);
+          mul_sub_x2(__uint_as_float(p01 << 16), __uint_as_float(p01 & 0xffff0000u),
+                     __uint_as_float(u[c][i]), __uint_as_float(u[c][i + 1]), d4.x, d4.y, ds[i],
+                     ds[i + 1]);
+          mul_sub_x2(__uint_as_float(p23 << 16), __uint_as_float(p23 & 0xffff0000u),
+                     __uint_as_float(u[c][i + 2]), __uint_as_float(u[c][i + 3]), d4.z, d4.w,
+                     ds[i + 2], ds[i + 3]);
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {  // four 16-byte chunks of 8 queries

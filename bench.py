@@ -45,6 +45,12 @@ def flops(B, H, N, d, causal):
     return f, 2.5 * f
 
 
+def job_tflops(world, step_flops, ms_per_step):
+    """Whole-job throughput: every rank runs one full workload per step, and
+    ms_per_step is the slowest rank's."""
+    return world * step_flops / (ms_per_step * 1e-3) / 1e12
+
+
 def measured_traffic(kernel):
     """DRAM bytes per launch of ``kernel`` from the committed ncu capture, or None
     when the kernel's sources changed since the counters were taken."""
@@ -313,7 +319,7 @@ def run_gpu(args):
     conv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in bwd_ev) if do_bwd else nan
     ms_per_step = elapsed_ms / K
     step_flops = (f_fwd if do_fwd else 0.0) + (f_bwd if do_bwd else 0.0)
-    value = world * step_flops / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(world, step_flops, ms_per_step)
     peak_tf, peak_hbm, peak_src = peaks()
 
     # the dominant kernel by time is the backward main kernel; its algorithmic
@@ -367,7 +373,7 @@ def run_gpu(args):
         torch.cuda.synchronize(device)
         barrier(world)
         e2e_ms = max_over_ranks(a.elapsed_time(b), world, device) / K
-        e2e = {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        e2e = {"value": job_tflops(world, step_flops, e2e_ms), "unit": UNIT,
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     cpu = None

@@ -9,6 +9,7 @@
 
 #include "../../include/fattn.h"
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace fattn {
 namespace {
@@ -206,6 +207,36 @@ extern "C" int fattn_tile_sizes(int d, int pass, int* block_q, int* block_k) {
   if (block_q) *block_q = bq;
   if (block_k) *block_k = bk;
   return FATTN_OK;
+}
+
+namespace fattn {
+namespace {
+// One warp waits on an mbarrier that nothing ever completes, through the same
+// bounded wait the attention kernels use, with a short limit: the wait gives
+// up, records ERR_SITE_CHECK | 1 in the error word and the kernel returns.
+__global__ void wait_timeout_check_kernel(long long limit, unsigned int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0u;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  WaitCtx ctx{&abort_flag, err, limit};
+  mbar_wait(smem_u32(&bar), 0, ctx, ERR_SITE_CHECK | 0x01);
+}
+}  // namespace
+}  // namespace fattn
+
+extern "C" int fattn_check_wait_timeout(long long limit_cycles, void* stream) {
+  if (limit_cycles < 1 || limit_cycles > FATTN_WAIT_TIMEOUT_CYCLES) return FATTN_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  const int st = current_device(&dev);
+  if (st != FATTN_OK) return st;
+  fattn::wait_timeout_check_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_cycles,
+                                                                                   dev->err);
+  return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
 extern "C" int fattn_device_error(unsigned int* code, int clear) {

@@ -11,6 +11,7 @@ namespace fattn {
 enum : uint32_t {
   ERR_SITE_FWD = 0x100,
   ERR_SITE_BWD = 0x200,
+  ERR_SITE_CHECK = 0x300,  // fattn_check_wait_timeout
 };
 
 struct FwdParams {

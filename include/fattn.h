@@ -133,14 +133,13 @@ int fattn_tile_sizes(int d, int pass, int* block_q, int* block_k);
 int fattn_device_error(unsigned int* code, int clear);
 
 /* Failure-path check: launches one warp that waits, through the kernels'
- * bounded-wait routine, on a barrier that nothing completes, giving up after
- * limit_cycles SM clock cycles (1 .. 4e9).  The wait then records code 0x301
+ * bounded-wait routine, on a barrier that nothing completes, with a short
+ * limit (2^21 SM clock cycles, about 1 ms).  The wait then records code 0x301
  * in the device error word (read it with fattn_device_error) and the kernel
  * returns; the context stays usable.  Asynchronous on stream.  Returns
- * FATTN_OK, FATTN_ERR_INVALID_ARG (limit out of range), FATTN_ERR_UNSUPPORTED
- * or FATTN_ERR_CUDA.  The pages have no counterpart; it tests this library's
- * own timeout reporting. */
-int fattn_check_wait_timeout(long long limit_cycles, void* stream);
+ * FATTN_OK, FATTN_ERR_UNSUPPORTED or FATTN_ERR_CUDA.  The pages have no
+ * counterpart; it tests this library's own timeout reporting. */
+int fattn_check_wait_timeout(void* stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* fattn_status_string(int status);

@@ -212,9 +212,11 @@ extern "C" int fattn_tile_sizes(int d, int pass, int* block_q, int* block_k) {
 namespace fattn {
 namespace {
 // One warp waits on an mbarrier that nothing ever completes, through the same
-// bounded wait the attention kernels use, with a short limit: the wait gives
-// up, records ERR_SITE_CHECK | 1 in the error word and the kernel returns.
-__global__ void wait_timeout_check_kernel(long long limit, unsigned int* err) {
+// bounded wait the attention kernels use, with a short limit (2^21 cycles,
+// about 1 ms): the wait gives up, records ERR_SITE_CHECK | 1 in the error word
+// and the kernel returns.
+constexpr long long kCheckLimitCycles = 1ll << 21;
+__global__ void wait_timeout_check_kernel(unsigned int* err) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t abort_flag;
   if (threadIdx.x == 0) {
@@ -223,19 +225,17 @@ __global__ void wait_timeout_check_kernel(long long limit, unsigned int* err) {
     fence_mbar_init();
   }
   __syncthreads();
-  WaitCtx ctx{&abort_flag, err, limit};
-  mbar_wait(smem_u32(&bar), 0, ctx, ERR_SITE_CHECK | 0x01);
+  WaitCtx ctx{&abort_flag, err};
+  mbar_wait<kCheckLimitCycles>(smem_u32(&bar), 0, ctx, ERR_SITE_CHECK | 0x01);
 }
 }  // namespace
 }  // namespace fattn
 
-extern "C" int fattn_check_wait_timeout(long long limit_cycles, void* stream) {
-  if (limit_cycles < 1 || limit_cycles > FATTN_WAIT_TIMEOUT_CYCLES) return FATTN_ERR_INVALID_ARG;
+extern "C" int fattn_check_wait_timeout(void* stream) {
   DeviceInfo* dev = nullptr;
   const int st = current_device(&dev);
   if (st != FATTN_OK) return st;
-  fattn::wait_timeout_check_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_cycles,
-                                                                                   dev->err);
+  fattn::wait_timeout_check_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev->err);
   return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 

@@ -1,7 +1,8 @@
 // ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarriers, TMA, tcgen05/TMEM.
 //
 // Every wait on an mbarrier is bounded: after FATTN_WAIT_TIMEOUT_CYCLES SM
-// clock cycles (or the shorter limit a WaitCtx carries) (%clock64: per-SM, monotonic, never adjusted by the driver) the
+// clock cycles (a template argument of the wait; the failure-path check uses a
+// shorter one) (%clock64: per-SM, monotonic, never adjusted by the driver) the
 // waiting thread records an error code in a device word, raises the CTA's
 // abort flag and returns false, so a kernel never spins forever.  Once the
 // abort flag is up, the kernels stop issuing new loads and MMAs, and each role
@@ -65,7 +66,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 struct WaitCtx {
   volatile uint32_t* abort_flag;  // shared
   unsigned int* err;              // global, may be null
-  long long limit = FATTN_WAIT_TIMEOUT_CYCLES;  // cycles before a wait gives up
 };
 
 // A translation unit may define FATTN_INLINE_WAIT_SLOW_PATH before including
@@ -76,6 +76,7 @@ struct WaitCtx {
 #else
 #define FATTN_WAIT_SLOW_ATTR __noinline__
 #endif
+template <long long kLimit>
 static __device__ FATTN_WAIT_SLOW_ATTR bool mbar_wait_slow(uint32_t bar, uint32_t parity,
                                                           const WaitCtx& ctx, uint32_t site,
                                                           bool drain) {
@@ -85,7 +86,7 @@ static __device__ FATTN_WAIT_SLOW_ATTR bool mbar_wait_slow(uint32_t bar, uint32_
     for (int i = 0; i < 256; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (!drain && *ctx.abort_flag) return false;
-    if (clock_cycles() - t0 > ctx.limit) {  // signed: immune to wrap
+    if (clock_cycles() - t0 > kLimit) {  // signed: immune to wrap
       *ctx.abort_flag = 1u;
       if (ctx.err) atomicCAS(ctx.err, 0u, site);
       return false;
@@ -95,10 +96,11 @@ static __device__ FATTN_WAIT_SLOW_ATTR bool mbar_wait_slow(uint32_t bar, uint32_
 
 // Wait for completion of the phase with the given parity; false on timeout,
 // or at once when the CTA is already aborting.
+template <long long kLimit = FATTN_WAIT_TIMEOUT_CYCLES>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
                                           uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, ctx, site, false);
+  return mbar_wait_slow<kLimit>(bar, parity, ctx, site, false);
 }
 
 // Wait for the CTA's own asynchronous work (TMA copies, MMAs) to finish, even
@@ -106,7 +108,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 __device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
                                            uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, ctx, site, true);
+  return mbar_wait_slow<FATTN_WAIT_TIMEOUT_CYCLES>(bar, parity, ctx, site, true);
 }
 
 __device__ __forceinline__ bool aborting(const WaitCtx& ctx) { return *ctx.abort_flag != 0u; }

@@ -36,7 +36,7 @@ SIGNATURES = {
                                _i, _vp]),
     "fattn_tile_sizes": (_i, [_i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "fattn_device_error": (_i, [ctypes.POINTER(ctypes.c_uint), _i]),
-    "fattn_check_wait_timeout": (_i, [ctypes.c_longlong, _vp]),
+    "fattn_check_wait_timeout": (_i, [_vp]),
     "fattn_status_string": (ctypes.c_char_p, [_i]),
 }
 
@@ -150,13 +150,13 @@ def fattn_device_error(clear=True):
     return code.value
 
 
-def check_wait_timeout(limit_cycles, stream=None):
+def check_wait_timeout(stream=None):
     """Launch the library's failure-path check (a bounded wait that must give up
-    after limit_cycles) on the current stream; read the outcome with
+    after about 1 ms) on the current stream; read the outcome with
     fattn_device_error()."""
     import torch
     s = stream if stream is not None else torch.cuda.current_stream().cuda_stream
-    _check("fattn_check_wait_timeout", load().fattn_check_wait_timeout(int(limit_cycles), s))
+    _check("fattn_check_wait_timeout", load().fattn_check_wait_timeout(s))
 
 
 def fattn_status_string(status):

@@ -22,7 +22,7 @@ CHECK_SITE = 0x301  # ERR_SITE_CHECK | 1
 
 def test_bounded_wait_reports_timeout_and_context_survives():
     assert fattn.fattn_device_error(clear=True) == 0
-    fattn.check_wait_timeout(2_000_000)  # about 1 ms at 2 GHz
+    fattn.check_wait_timeout()  # gives up after about 1 ms
     torch.cuda.synchronize()
     assert fattn.fattn_device_error(clear=True) == CHECK_SITE
     assert fattn.fattn_device_error(clear=True) == 0  # reading with clear resets it
@@ -42,8 +42,8 @@ def test_bounded_wait_reports_timeout_and_context_survives():
 
 
 def test_first_failure_wins():
-    fattn.check_wait_timeout(1_000_000)
-    fattn.check_wait_timeout(1_000_000)
+    fattn.check_wait_timeout()
+    fattn.check_wait_timeout()
     torch.cuda.synchronize()
     assert fattn.fattn_device_error(clear=False) == CHECK_SITE
     assert fattn.fattn_device_error(clear=True) == CHECK_SITE

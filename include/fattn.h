@@ -102,6 +102,36 @@ int fattn_bwd_ex(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, void* workspace, size_t workspace_bytes,
                  void* const* phase_events, void* stream);
 
+/* Variable-length batches (padded attention without the padding: "Causal
+ * masking fits inside the tiled computation" on page "FlashAttention tiles
+ * exact softmax without materializing the score matrix" masks positions
+ * inside a tile; here each sequence simply ends where its length says).
+ * B sequences of lengths n_b = cu_seqlens[b+1] - cu_seqlens[b] are packed
+ * head-major: q, k, v, o, dout, dq, dk, dv are DEVICE pointers to bf16
+ * [H, total, d] (sequence b at rows [cu_seqlens[b], cu_seqlens[b+1]) of every
+ * head) and lse is fp32 [H, total].  Each sequence is its own attention
+ * problem: its queries see only its own keys (and, causal, only keys at or
+ * before their own position in the sequence).
+ * cu_seqlens: DEVICE int32 array of B+1 non-decreasing offsets, cu_seqlens[0]
+ * = 0 and cu_seqlens[B] = total; max_seqlen >= every n_b (the grid is sized by
+ * it); total is passed by the caller because the host cannot read device
+ * memory without a synchronisation.  Entries are checked on the device: a
+ * sequence that is out of range, decreasing or longer than max_seqlen is
+ * skipped and reported through the device error word (code 0x140 forward,
+ * 0x240 backward).  Empty sequences are allowed; total == 0 launches nothing.
+ * Returns as fattn_fwd; tile counters are not available. */
+int fattn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                     const int* cu_seqlens, int B, int H, int max_seqlen, int total, int d,
+                     float scale, int causal, void* stream);
+
+/* Backward of fattn_fwd_varlen: the layouts above; workspace of at least
+ * fattn_bwd_workspace_bytes(1, H, total, d) bytes.  Returns as fattn_bwd. */
+int fattn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                     const int* cu_seqlens, int B, int H, int max_seqlen, int total, int d,
+                     float scale, int causal, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
 /* Size of the device array that fattn_bwd_noalloc uses as its workspace. */
 #define FATTN_NOALLOC_SCRATCH_BYTES (64u << 20)
 

@@ -94,75 +94,80 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 using namespace fattn;
 
-extern "C" int fattn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
-                            int B, int H, int N, int d, float scale, int causal,
-                            unsigned long long* tile_counts, void* stream) {
-  int st = check_common(B, H, N, d, scale);
-  if (st != FATTN_OK) return st;
+namespace fattn {
+namespace {
+
+// Geometry of one call: the TMA maps span `map_rows` rows of `map_z` slices
+// ([B*H, N, d] dense, [H, T, d] varlen); kernels see p.N = the (longest)
+// sequence length and the varlen table, if any.
+struct Geometry {
+  long long map_rows;
+  long long map_z;
+  int BH;        // units the dense grid iterates over (B*H; H when varlen)
+  int N;         // sequence length, or the longest one when varlen
+  Varlen vl;
+};
+
+int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int d, float scale,
+            int causal, const Geometry& g, unsigned long long* tile_counts, void* stream) {
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FATTN_ERR_INVALID_ARG;
   if (tile_counts && (reinterpret_cast<uintptr_t>(tile_counts) & 7u)) return FATTN_ERR_INVALID_ARG;
   DeviceInfo* dev = nullptr;
-  st = current_device(&dev);
+  const int st = current_device(&dev);
   if (st != FATTN_OK) return st;
-  const long long BH = (long long)B * H;
   CUtensorMap tq, tk, tv, to;
-  if (!make_bf16_map(&tq, q, d, N, BH, 128) || !make_bf16_map(&tk, k, d, N, BH, 128) ||
-      !make_bf16_map(&tv, v, d, N, BH, 128) || !make_bf16_map(&to, o, d, N, BH, 128))
+  if (!make_bf16_map(&tq, q, d, g.map_rows, g.map_z, 128) ||
+      !make_bf16_map(&tk, k, d, g.map_rows, g.map_z, 128) ||
+      !make_bf16_map(&tv, v, d, g.map_rows, g.map_z, 128) ||
+      !make_bf16_map(&to, o, d, g.map_rows, g.map_z, 128))
     return FATTN_ERR_CUDA;
-  FwdParams p;
-  p.BH = (int)BH;
-  p.N = N;
+  FwdParams p{};
+  p.BH = g.BH;
+  p.N = g.N;
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.lse = lse;
   p.tiles = tile_counts;
   p.err = dev->err;
+  p.vl = g.vl;
+  p.o = static_cast<uint16_t*>(o);
   cudaError_t e = launch_fwd(d, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
-extern "C" int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                         int H, int N, int d, float scale, int causal, void* stream) {
-  return fattn_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, nullptr, stream);
+size_t workspace_bytes_for_rows(long long rows, int d) {
+  return align256((size_t)rows * d * sizeof(float)) + align256((size_t)rows * sizeof(float));
 }
 
-extern "C" size_t fattn_bwd_workspace_bytes(int B, int H, int N, int d) {
-  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
-  const size_t rows = (size_t)B * H * N;
-  return align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
-}
-
-extern "C" int fattn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
-                            const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                            int B, int H, int N, int d, float scale, int causal, void* workspace,
-                            size_t workspace_bytes, void* const* phase_events, void* stream) {
-  int st = check_common(B, H, N, d, scale);
-  if (st != FATTN_OK) return st;
+int run_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+            const void* dout, void* dq, void* dk, void* dv, int d, float scale, int causal,
+            const Geometry& g, void* workspace, size_t workspace_bytes,
+            void* const* phase_events, void* stream) {
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FATTN_ERR_INVALID_ARG;
-  const size_t need = fattn_bwd_workspace_bytes(B, H, N, d);
+  const long long rows = g.map_rows * g.map_z;
+  const size_t need = workspace_bytes_for_rows(rows, d);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
     return FATTN_ERR_WORKSPACE;
   DeviceInfo* dev = nullptr;
-  st = current_device(&dev);
+  const int st = current_device(&dev);
   if (st != FATTN_OK) return st;
-  const long long BH = (long long)B * H;
-  const long long rows = BH * N;
   float* dq_acc = static_cast<float*>(workspace);
   float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                           align256((size_t)rows * d * sizeof(float)));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int bq = 0, bk = 0;
   fattn_tile_sizes(d, 1, &bq, &bk);
+  const long long R = g.map_rows, Z = g.map_z;
   CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
-  if (!make_bf16_map(&tq, q, d, N, BH, bq) || !make_bf16_map(&tdo, dout, d, N, BH, bq) ||
-      !make_bf16_map(&tk, k, d, N, BH, bk) || !make_bf16_map(&tv, v, d, N, BH, bk) ||
-      !make_bf16_map(&tdk, dk, d, N, BH, bk) || !make_bf16_map(&tdv, dv, d, N, BH, bk))
+  if (!make_bf16_map(&tq, q, d, R, Z, bq) || !make_bf16_map(&tdo, dout, d, R, Z, bq) ||
+      !make_bf16_map(&tk, k, d, R, Z, bk) || !make_bf16_map(&tv, v, d, R, Z, bk) ||
+      !make_bf16_map(&tdk, dk, d, R, Z, bk) || !make_bf16_map(&tdv, dv, d, R, Z, bk))
     return FATTN_ERR_CUDA;
   // dQ accumulator: fp32, add-reduced 16 query rows at a time
-  if (!make_map(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, BH, d, 16,
+  if (!make_map(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, R, Z, d, 16,
                 CU_TENSOR_MAP_SWIZZLE_NONE))
     return FATTN_ERR_CUDA;
   auto mark = [&](int i) {
@@ -173,9 +178,9 @@ extern "C" int fattn_bwd_ex(const void* q, const void* k, const void* v, const v
   if (launch_bwd_preprocess(o, dout, delta, dq_acc, rows, d, s) != cudaSuccess)
     return FATTN_ERR_CUDA;
   if (!mark(1)) return FATTN_ERR_CUDA;
-  BwdParams p;
-  p.BH = (int)BH;
-  p.N = N;
+  BwdParams p{};
+  p.BH = g.BH;
+  p.N = g.N;
   p.causal = causal ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -183,6 +188,9 @@ extern "C" int fattn_bwd_ex(const void* q, const void* k, const void* v, const v
   p.delta = delta;
   p.dq_acc = dq_acc;
   p.err = dev->err;
+  p.vl = g.vl;
+  p.dk = static_cast<uint16_t*>(dk);
+  p.dv = static_cast<uint16_t*>(dv);
   cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, tdk, tdv, tdq, p, s);
   if (e == cudaErrorNotSupported) return FATTN_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return FATTN_ERR_CUDA;
@@ -190,6 +198,75 @@ extern "C" int fattn_bwd_ex(const void* q, const void* k, const void* v, const v
   if (launch_bwd_convert(dq_acc, dq, rows * d, scale, s) != cudaSuccess) return FATTN_ERR_CUDA;
   if (!mark(3)) return FATTN_ERR_CUDA;
   return FATTN_OK;
+}
+
+Geometry dense_geometry(int B, int H, int N) {
+  return Geometry{N, (long long)B * H, B * H, N, Varlen{nullptr, 0, 0, 0}};
+}
+
+// Varlen arguments: B sequences, H heads, T total rows, the longest sequence
+// max_seqlen; cu_seqlens is checked entry by entry on the device.
+int check_varlen(const int* cu_seqlens, int B, int H, int max_seqlen, int T, int d, float scale) {
+  if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return FATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || max_seqlen < 0 || T < 0 || max_seqlen > T) return FATTN_ERR_INVALID_ARG;
+  if ((long long)H * T >= (1LL << 31)) return FATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  return FATTN_OK;
+}
+
+}  // namespace
+}  // namespace fattn
+
+extern "C" int fattn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int H, int N, int d, float scale, int causal,
+                            unsigned long long* tile_counts, void* stream) {
+  const int st = check_common(B, H, N, d, scale);
+  if (st != FATTN_OK) return st;
+  return run_fwd(q, k, v, o, lse, d, scale, causal, dense_geometry(B, H, N), tile_counts, stream);
+}
+
+extern "C" int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int d, float scale, int causal, void* stream) {
+  return fattn_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, nullptr, stream);
+}
+
+extern "C" int fattn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                                const int* cu_seqlens, int B, int H, int max_seqlen, int total,
+                                int d, float scale, int causal, void* stream) {
+  const int st = check_varlen(cu_seqlens, B, H, max_seqlen, total, d, scale);
+  if (st != FATTN_OK) return st;
+  if (total == 0 || max_seqlen == 0) return FATTN_OK;  // no rows: nothing to compute
+  const Geometry g{total, H, H, max_seqlen, Varlen{cu_seqlens, B, H, total}};
+  return run_fwd(q, k, v, o, lse, d, scale, causal, g, nullptr, stream);
+}
+
+extern "C" size_t fattn_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  return workspace_bytes_for_rows((long long)B * H * N, d);
+}
+
+extern "C" int fattn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                            int B, int H, int N, int d, float scale, int causal, void* workspace,
+                            size_t workspace_bytes, void* const* phase_events, void* stream) {
+  const int st = check_common(B, H, N, d, scale);
+  if (st != FATTN_OK) return st;
+  return run_bwd(q, k, v, o, lse, dout, dq, dk, dv, d, scale, causal, dense_geometry(B, H, N),
+                 workspace, workspace_bytes, phase_events, stream);
+}
+
+extern "C" int fattn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                                const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                const int* cu_seqlens, int B, int H, int max_seqlen, int total,
+                                int d, float scale, int causal, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  const int st = check_varlen(cu_seqlens, B, H, max_seqlen, total, d, scale);
+  if (st != FATTN_OK) return st;
+  if (total == 0 || max_seqlen == 0) return FATTN_OK;  // no rows: nothing to compute
+  const Geometry g{total, H, H, max_seqlen, Varlen{cu_seqlens, B, H, total}};
+  return run_bwd(q, k, v, o, lse, dout, dq, dk, dv, d, scale, causal, g, workspace,
+                 workspace_bytes, nullptr, stream);
 }
 
 extern "C" int fattn_bwd(const void* q, const void* k, const void* v, const void* o,

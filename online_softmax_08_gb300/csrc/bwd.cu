@@ -143,7 +143,9 @@ __device__ __forceinline__ void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-template <int D>
+// VARLEN: the CTA's sequence comes from p.vl.cu_seqlens (packed head-major
+// rows); otherwise the dense [B, H, N, d] layout.
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
     fattn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -160,9 +162,22 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
   uint8_t* smem = smem_raw + (sbase - raw);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int N = p.N;
-  const int kb = (int)(blockIdx.x / (unsigned)p.BH);  // key block; causal: heaviest first
-  const int bh = (int)(blockIdx.x % (unsigned)p.BH);
+  const int units = VARLEN ? p.vl.B * p.vl.H : p.BH;
+  const int kb = (int)(blockIdx.x / (unsigned)units);  // key block; causal: heaviest first
+  const int unit = (int)(blockIdx.x % (unsigned)units);
+  SeqView seq;
+  if constexpr (VARLEN) {
+    if (!seq_view(p.vl, p.N, unit / p.vl.H, unit % p.vl.H, unit, p.N, &seq)) {
+      if (threadIdx.x == 0 && p.err) atomicCAS(p.err, 0u, (unsigned)(ERR_SITE_BWD | 0x40));
+      return;
+    }
+    if (kb * C::BK >= seq.N) return;  // this sequence is shorter: nothing to do
+  } else {
+    seq = SeqView{p.N, 0, unit, (long long)unit * p.N};
+  }
+  const int N = seq.N;
+  const int bh = seq.z;        // TMA z coordinate
+  const int row0 = seq.row0;   // first row of the sequence in the tensor
   const int k0 = kb * C::BK;
   const int n_qb = (N + BQ - 1) / BQ;
   const int i_start = p.causal ? k0 / BQ : 0;
@@ -213,8 +228,8 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
         tma_prefetch_desc(&tm_do);
         mbar_arrive_expect_tx(bar(B_KV), 2 * C::TILE);
         for (int h = 0; h < D / 64; ++h) {
-          tma_load_3d(sbase + C::OFF_K + h * C::HALF, &tm_k, bar(B_KV), h * 64, k0, bh);
-          tma_load_3d(sbase + C::OFF_V + h * C::HALF, &tm_v, bar(B_KV), h * 64, k0, bh);
+          tma_load_3d(sbase + C::OFF_K + h * C::HALF, &tm_k, bar(B_KV), h * 64, row0 + k0, bh);
+          tma_load_3d(sbase + C::OFF_V + h * C::HALF, &tm_v, bar(B_KV), h * 64, row0 + k0, bh);
         }
       }
       const float kLog2e = 1.4426950408889634f;
@@ -233,7 +248,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
             mbar_arrive_expect_tx(bar(B_Q_FULL + st), C::TILE);
             for (int h = 0; h < D / 64; ++h)
               tma_load_3d(sbase + C::OFF_Q + st * C::TILE + h * C::HALF, &tm_q,
-                          bar(B_Q_FULL + st), h * 64, q0, bh);
+                          bar(B_Q_FULL + st), h * 64, row0 + q0, bh);
           }
           q_issued = it + 1;
           float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT + st * 2 * BQ * 4);
@@ -242,8 +257,8 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
           for (int j = 0; j < BQ / 32; ++j) {
             const int q = q0 + lane + 32 * j;
             // -LSE2; a query past N gets -inf, so its P column is exactly zero
-            l[j] = q < N ? -p.lse[(size_t)bh * N + q] * kLog2e : -INFINITY;
-            dl[j] = q < N ? p.delta[(size_t)bh * N + q] : 0.f;
+            l[j] = q < N ? -p.lse[seq.stat0 + q] * kLog2e : -INFINITY;
+            dl[j] = q < N ? p.delta[seq.stat0 + q] : 0.f;
           }
 #pragma unroll
           for (int j = 0; j < BQ / 32; ++j) {
@@ -261,7 +276,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
             mbar_arrive_expect_tx(bar(B_O_FULL + so), C::TILE);
             for (int h = 0; h < D / 64; ++h)
               tma_load_3d(sbase + C::OFF_DO + so * C::TILE + h * C::HALF, &tm_do,
-                          bar(B_O_FULL + so), h * 64, q0, bh);
+                          bar(B_O_FULL + so), h * 64, row0 + q0, bh);
           }
           o_issued = it + 1;
         }
@@ -398,7 +413,10 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
         fence_proxy_async_smem();
         named_bar_sync(2, 128);
         if (t == 0) {
-          tma_reduce_add_3d(&tm_dq, buf, 0, q0 + 16 * h, bh);
+          // rows past the sequence end belong to the next one (or lie past the
+          // tensor, where TMA clips them): their partial is exactly zero, since
+          // their LSE is +inf, so adding it changes nothing
+          tma_reduce_add_3d(&tm_dq, buf, 0, row0 + q0 + 16 * h, bh);
           bulk_commit();
         }
       }
@@ -548,15 +566,36 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
         }
       }
     }
-    fence_proxy_async_smem();
-    named_bar_sync(1, 256);
-    if (ctid == 0) {
-      for (int h = 0; h < D / 64; ++h) {
-        tma_store_3d(&tm_dk, sbase + C::OFF_K + h * C::HALF, h * 64, k0, bh);
-        tma_store_3d(&tm_dv, sbase + C::OFF_V + h * C::HALF, h * 64, k0, bh);
+    if (VARLEN && k0 + C::BK > N) {
+      // the block runs past the end of the sequence, into the next one's rows:
+      // thread (which, t) writes row t of dK or dV if it belongs to the sequence
+      named_bar_sync(1, 256);
+      const int which = ctid >> 7;
+      if (k0 + t < N) {
+        const uint32_t src = sbase + (which == 0 ? C::OFF_K : C::OFF_V);
+        uint4* dst = reinterpret_cast<uint4*>((which == 0 ? p.dk : p.dv) +
+                                              ((size_t)bh * p.vl.T + row0 + k0 + t) * D);
+#pragma unroll
+        for (int c16 = 0; c16 < D / 8; ++c16) {
+          const int half = c16 >> 3, chunk = c16 & 7;
+          uint4 v4;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(v4.x), "=r"(v4.y), "=r"(v4.z), "=r"(v4.w)
+                       : "r"(src + half * C::HALF + t * 128 + ((chunk ^ (t & 7)) << 4)));
+          dst[c16] = v4;
+        }
       }
-      bulk_commit();
-      bulk_wait_all();
+    } else {
+      fence_proxy_async_smem();
+      named_bar_sync(1, 256);
+      if (ctid == 0) {
+        for (int h = 0; h < D / 64; ++h) {
+          tma_store_3d(&tm_dk, sbase + C::OFF_K + h * C::HALF, h * 64, row0 + k0, bh);
+          tma_store_3d(&tm_dv, sbase + C::OFF_V + h * C::HALF, h * 64, row0 + k0, bh);
+        }
+        bulk_commit();
+        bulk_wait_all();
+      }
     }
     __syncwarp();
   }
@@ -569,27 +608,28 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
   }
 }
 
-template <int D>
+template <int D, bool VARLEN>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                    const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                    const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
   using C = Bwd<D>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
   static_assert(C::TM_Y + 128 <= 512, "TMEM budget");
-  cudaError_t e = cudaFuncSetAttribute(fattn_bwd_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(fattn_bwd_kernel<D, VARLEN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   // the setmaxnreg split hands out exactly the launch's registers (128 per thread);
   // with fewer at launch an increase would never be granted
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, fattn_bwd_kernel<D>);
+  e = cudaFuncGetAttributes(&fa, fattn_bwd_kernel<D, VARLEN>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != 128) return cudaErrorInvalidConfiguration;
   const long long n_kb = (p.N + C::BK - 1) / C::BK;
-  const long long blocks = n_kb * p.BH;
+  const long long blocks = n_kb * (VARLEN ? (long long)p.vl.B * p.vl.H : p.BH);
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fattn_bwd_kernel<D><<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdk,
-                                                                          tdv, tdq, p);
+  if (blocks == 0) return cudaSuccess;
+  fattn_bwd_kernel<D, VARLEN><<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(
+      tq, tk, tv, tdo, tdk, tdv, tdq, p);
   return cudaGetLastError();
 }
 
@@ -599,8 +639,11 @@ cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
                             const CUtensorMap& tdk, const CUtensorMap& tdv,
                             const CUtensorMap& tdq_acc, const BwdParams& p, cudaStream_t stream) {
-  if (d == 128) return launch<128>(tq, tk, tv, tdo, tdk, tdv, tdq_acc, p, stream);
-  if (d == 64) return launch<64>(tq, tk, tv, tdo, tdk, tdv, tdq_acc, p, stream);
+  const bool vl = p.vl.cu_seqlens != nullptr;
+  if (d == 128) return vl ? launch<128, true>(tq, tk, tv, tdo, tdk, tdv, tdq_acc, p, stream)
+                          : launch<128, false>(tq, tk, tv, tdo, tdk, tdv, tdq_acc, p, stream);
+  if (d == 64) return vl ? launch<64, true>(tq, tk, tv, tdo, tdk, tdv, tdq_acc, p, stream)
+                         : launch<64, false>(tq, tk, tv, tdo, tdk, tdv, tdq_acc, p, stream);
   return cudaErrorInvalidValue;
 }
 

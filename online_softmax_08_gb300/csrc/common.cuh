@@ -14,14 +14,26 @@ enum : uint32_t {
   ERR_SITE_CHECK = 0x300,  // fattn_check_wait_timeout
 };
 
+// Variable-length batches: B sequences packed head-major, [H, T, d] with
+// sequence b at rows [cu_seqlens[b], cu_seqlens[b+1]) of every head (T =
+// cu_seqlens[B]).  Null cu_seqlens means the dense [B, H, N, d] layout.
+struct Varlen {
+  const int* cu_seqlens;      // device, B + 1 entries, or null
+  int B;                      // sequences
+  int H;                      // heads
+  int T;                      // total rows per head
+};
+
 struct FwdParams {
   int BH;                     // batch * heads
-  int N;                      // sequence length (queries == keys)
+  int N;                      // sequence length (queries == keys); the longest one when varlen
   int causal;                 // key j visible to query i iff j <= i
   float scale_log2;           // scale * log2(e): scores are taken to base 2
   float* lse;                 // [BH, N] fp32, natural-log units
   unsigned long long* tiles;  // optional [3]: full, masked, skipped (may be null)
   unsigned int* err;          // device error word
+  Varlen vl;
+  uint16_t* o;                // O (bf16 bits); varlen writes the last tile of a sequence row by row
 };
 
 struct BwdParams {
@@ -34,7 +46,38 @@ struct BwdParams {
   const float* delta;         // [BH, N] D_i = rowsum(dO o O)
   float* dq_acc;              // [BH, N, d] fp32 dQ accumulator (zeroed by the preprocess kernel)
   unsigned int* err;
+  Varlen vl;
+  uint16_t* dk;               // dK, dV (bf16 bits); varlen writes the last key block of a
+  uint16_t* dv;               // sequence row by row
 };
+
+// Where a CTA's sequence lives: its length, its first row in the tensor's
+// row dimension, the TMA z coordinate (b*H + h dense, h varlen), and the base
+// row of its per-row statistics (LSE, D).  Returns false for a bad
+// cu_seqlens entry (recorded in the error word by the caller).
+struct SeqView {
+  int N;
+  int row0;
+  int z;
+  long long stat0;
+};
+__device__ __forceinline__ bool seq_view(const Varlen& vl, int dense_N, int seq, int head,
+                                         int dense_bh, int max_len, SeqView* v) {
+  if (vl.cu_seqlens == nullptr) {
+    v->N = dense_N;
+    v->row0 = 0;
+    v->z = dense_bh;
+    v->stat0 = (long long)dense_bh * dense_N;
+    return true;
+  }
+  const int a = vl.cu_seqlens[seq], b = vl.cu_seqlens[seq + 1];
+  if (a < 0 || b < a || b > vl.T || b - a > max_len) return false;
+  v->N = b - a;
+  v->row0 = a;
+  v->z = head;
+  v->stat0 = (long long)head * vl.T + a;
+  return true;
+}
 
 // Launchers (one per translation unit).  Return cudaSuccess or the launch error.
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

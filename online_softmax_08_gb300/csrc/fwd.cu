@@ -63,7 +63,9 @@ enum {
   B_KV_FULL = 8,  // [STAGES], then kv_empty [STAGES]
 };
 
-template <int D>
+// VARLEN: the CTA's sequence comes from p.vl.cu_seqlens (packed head-major
+// rows); otherwise the dense [B, H, N, d] layout.
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
     fattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -77,11 +79,24 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
   uint8_t* smem = smem_raw + (sbase - raw);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int N = p.N;
-  const int n_qb = (N + 255) / 256;
+  const int n_qb = (p.N + 255) / 256;  // p.N: the (longest) sequence length
   // heaviest (last) query blocks first
-  const int qb = n_qb - 1 - (int)(blockIdx.x / (unsigned)p.BH);
-  const int bh = (int)(blockIdx.x % (unsigned)p.BH);
+  const int units = VARLEN ? p.vl.B * p.vl.H : p.BH;
+  const int qb = n_qb - 1 - (int)(blockIdx.x / (unsigned)units);
+  const int unit = (int)(blockIdx.x % (unsigned)units);
+  SeqView seq;
+  if constexpr (VARLEN) {
+    if (!seq_view(p.vl, p.N, unit / p.vl.H, unit % p.vl.H, unit, p.N, &seq)) {
+      if (threadIdx.x == 0 && p.err) atomicCAS(p.err, 0u, (unsigned)(ERR_SITE_FWD | 0x40));
+      return;
+    }
+    if (qb * 256 >= seq.N) return;  // this sequence is shorter: nothing to do
+  } else {
+    seq = SeqView{p.N, 0, unit, (long long)unit * p.N};
+  }
+  const int N = seq.N;
+  const int bh = seq.z;        // TMA z coordinate
+  const int row0 = seq.row0;   // first row of the sequence in the tensor
   const int n_kv_total = (N + C::BN - 1) / C::BN;
 
   // rows [r0_s, r0_s + 128) of subtile s see key tiles [0, nt_s)
@@ -140,7 +155,7 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
         if (nt[s] > 0)
           for (int h = 0; h < D / 64; ++h)
             tma_load_3d(sbase + C::OFF_Q + s * C::TILE + h * C::HALF, &tm_q, bar(B_Q), h * 64,
-                        r0[s], bh);
+                        row0 + r0[s], bh);
       const int n_loads = 2 * n_max;
       int issued = 0;
       for (int i = 0; i < n_loads; ++i) {
@@ -153,7 +168,8 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
         const CUtensorMap* m = (i & 1) ? &tm_v : &tm_k;
         mbar_arrive_expect_tx(kv_full0 + 8u * slot, C::TILE);
         for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(dst + h * C::HALF, m, kv_full0 + 8u * slot, h * 64, (i >> 1) * C::BN, bh);
+          tma_load_3d(dst + h * C::HALF, m, kv_full0 + 8u * slot, h * 64, row0 + (i >> 1) * C::BN,
+                      bh);
         issued = i + 1;
       }
       // drain: at most one load per slot can still be landing, the latest one
@@ -353,14 +369,32 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
                        pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
         }
       }
-      fence_proxy_async_smem();
-      named_bar_sync(1 + s, 128);
-      if (t == 0) {
-        for (int h = 0; h < D / 64; ++h) tma_store_3d(&tm_o, o_base + h * C::HALF, h * 64, my_r0, bh);
-        bulk_commit();
-        bulk_wait_all();
+      if (VARLEN && my_r0 + C::BM > N) {
+        // the tile runs past the end of the sequence, into the next one's rows:
+        // each thread writes its own row if it belongs to the sequence
+        if (row < N) {
+          uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.vl.T + row0 + row) * D);
+#pragma unroll
+          for (int c16 = 0; c16 < D / 8; ++c16) {
+            const int half = c16 >> 3, chunk = c16 & 7;
+            uint4 v4;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v4.x), "=r"(v4.y), "=r"(v4.z), "=r"(v4.w)
+                         : "r"(o_base + half * C::HALF + t * 128 + ((chunk ^ (t & 7)) << 4)));
+            dst[c16] = v4;
+          }
+        }
+      } else {
+        fence_proxy_async_smem();
+        named_bar_sync(1 + s, 128);
+        if (t == 0) {
+          for (int h = 0; h < D / 64; ++h)
+            tma_store_3d(&tm_o, o_base + h * C::HALF, h * 64, row0 + my_r0, bh);
+          bulk_commit();
+          bulk_wait_all();
+        }
       }
-      if (row < N) p.lse[(size_t)bh * N + row] = (m_run * sl2 + lg2(l_run)) * kLn2;
+      if (row < N) p.lse[seq.stat0 + row] = (m_run * sl2 + lg2(l_run)) * kLn2;
       if (p.tiles && t == 0) {
         atomicAdd(p.tiles + 0, n_full);
         atomicAdd(p.tiles + 1, n_masked);
@@ -378,18 +412,19 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
   }
 }
 
-template <int D>
+template <int D, bool VARLEN>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                    const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
   using C = Fwd<D>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(fattn_fwd_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(fattn_fwd_kernel<D, VARLEN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const long long n_qb = (p.N + 255) / 256;
-  const long long blocks = n_qb * p.BH;
+  const long long blocks = n_qb * (VARLEN ? (long long)p.vl.B * p.vl.H : p.BH);
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fattn_fwd_kernel<D><<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, to, p);
+  if (blocks == 0) return cudaSuccess;
+  fattn_fwd_kernel<D, VARLEN><<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
@@ -397,8 +432,11 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
-  if (d == 128) return launch<128>(tq, tk, tv, to, p, stream);
-  if (d == 64) return launch<64>(tq, tk, tv, to, p, stream);
+  const bool vl = p.vl.cu_seqlens != nullptr;
+  if (d == 128) return vl ? launch<128, true>(tq, tk, tv, to, p, stream)
+                          : launch<128, false>(tq, tk, tv, to, p, stream);
+  if (d == 64) return vl ? launch<64, true>(tq, tk, tv, to, p, stream)
+                         : launch<64, false>(tq, tk, tv, to, p, stream);
   return cudaErrorInvalidValue;
 }
 

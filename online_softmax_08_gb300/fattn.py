@@ -37,6 +37,9 @@ SIGNATURES = {
     "fattn_tile_sizes": (_i, [_i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "fattn_device_error": (_i, [ctypes.POINTER(ctypes.c_uint), _i]),
     "fattn_check_wait_timeout": (_i, [_vp]),
+    "fattn_fwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "fattn_bwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
+                              _i, _f, _i, _vp, _sz, _vp]),
     "fattn_status_string": (ctypes.c_char_p, [_i]),
 }
 
@@ -138,6 +141,21 @@ def fattn_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal
         N, d, float(scale), int(bool(causal)), _stream(stream)))
 
 
+def fattn_fwd_varlen(q, k, v, o, lse, cu_seqlens, B, H, max_seqlen, total, d, scale, causal,
+                     stream=None):
+    _check("fattn_fwd_varlen", load().fattn_fwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens), B, H, int(max_seqlen),
+        int(total), d, float(scale), int(bool(causal)), _stream(stream)))
+
+
+def fattn_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, cu_seqlens, B, H, max_seqlen, total, d,
+                     scale, causal, workspace, workspace_bytes, stream=None):
+    _check("fattn_bwd_varlen", load().fattn_bwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+        _ptr(cu_seqlens), B, H, int(max_seqlen), int(total), d, float(scale), int(bool(causal)),
+        _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
 def fattn_tile_sizes(d, pass_):
     bq, bk = ctypes.c_int(0), ctypes.c_int(0)
     _check("fattn_tile_sizes", load().fattn_tile_sizes(d, pass_, ctypes.byref(bq), ctypes.byref(bk)))
@@ -192,4 +210,29 @@ def backward(q, k, v, o, lse, do, scale, causal, workspace=None, stream=None):
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     fattn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, workspace,
               workspace.numel() * workspace.element_size(), stream)
+    return dq, dk, dv
+
+
+def forward_varlen(q, k, v, cu_seqlens, max_seqlen, scale, causal, stream=None):
+    """O, LSE of packed bf16 [H, total, d] device tensors; cu_seqlens is a device
+    int32 tensor of B + 1 offsets (its last entry, total, is q.shape[1])."""
+    H, T, d = q.shape
+    B = cu_seqlens.numel() - 1
+    o = torch.empty_like(q)
+    lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    fattn_fwd_varlen(q, k, v, o, lse, cu_seqlens, B, H, max_seqlen, T, d, scale, causal, stream)
+    return o, lse
+
+
+def backward_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen, scale, causal, workspace=None,
+                    stream=None):
+    """dQ, dK, dV of forward_varlen for dL/dO = do."""
+    H, T, d = q.shape
+    B = cu_seqlens.numel() - 1
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = torch.empty(max(fattn_bwd_workspace_bytes(1, H, max(T, 1), d), 1),
+                                dtype=torch.uint8, device=q.device)
+    fattn_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, cu_seqlens, B, H, max_seqlen, T, d, scale,
+                     causal, workspace, workspace.numel() * workspace.element_size(), stream)
     return dq, dk, dv

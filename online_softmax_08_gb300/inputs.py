@@ -74,3 +74,26 @@ def sample_rows(N, count, seed, always=(0, 127, 128)):
     rows = [r for r in always if r < N] + [N - 1]
     extra = torch.randint(0, N, (max(0, count - len(rows)),), generator=g).tolist()
     return sorted(set(rows + extra))
+
+
+def make_varlen_inputs(lengths, H, d, seed, with_do=False):
+    """Packed variable-length batch: bf16 CPU tensors (q, k, v[, do]) of shape
+    [H, T, d] (sequence b at rows [cu[b], cu[b+1]) of every head, T = sum of
+    lengths) and the int32 offsets cu [B + 1].  Values ~ N(0, 1), drawn in fp32
+    in the order Q, K, V, dO."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    T = int(sum(lengths))
+    shape = (H, T, d)
+    out = [torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+           for _ in range(4 if with_do else 3)]
+    cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    return tuple(out) + (cu,)
+
+
+def varlen_lengths(B, lo, hi, seed):
+    """B sequence lengths drawn uniformly from [lo, hi] (a seeded length mix)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return torch.randint(lo, hi + 1, (B,), generator=g).tolist()

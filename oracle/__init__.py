@@ -11,6 +11,9 @@ compiles it on demand with gcc and marshals numpy arrays through ctypes.
   attention_fwd_rows  -- the same definition for sampled (head, query row) pairs
   attention_bwd       -- the textbook backward (dQ, dK, dV) of that definition
   tile_counts         -- brute-force full / masked / skipped tile classification
+  attention_fwd_varlen, attention_bwd_varlen
+                      -- packed variable-length batches: each sequence is its own
+                         attention problem (the definition applied per sequence)
 
 Inputs are numpy float64 arrays of shape [B, H, N, d] (contiguous).
 """
@@ -143,3 +146,40 @@ def tile_counts(N, causal, block_q, block_k):
     out, op = _i64(np.zeros(3))
     _check(lib.oracle_tile_counts(int(N), int(bool(causal)), int(block_q), int(block_k), op), "tiles")
     return tuple(int(x) for x in out)
+
+
+def _sequences(cu_seqlens):
+    cu = [int(x) for x in cu_seqlens]
+    if cu[0] != 0 or any(b < a for a, b in zip(cu, cu[1:])):
+        raise ValueError("cu_seqlens must start at 0 and not decrease")
+    return list(zip(cu[:-1], cu[1:]))
+
+
+def attention_fwd_varlen(q, k, v, cu_seqlens, scale, causal, nthreads=0):
+    """O [H,T,d] and LSE [H,T] of a packed batch: q, k, v are [H, T, d] with
+    sequence b at rows [cu[b], cu[b+1]).  Each sequence is an independent
+    attention problem; the definition (attention_fwd) is applied to each slice.
+    Rows that belong to no sequence (none, when cu[-1] == T) stay NaN."""
+    H, T, d = q.shape
+    o = np.full((H, T, d), np.nan)
+    lse = np.full((H, T), np.nan)
+    for a, b in _sequences(cu_seqlens):
+        if b == a:
+            continue
+        sl = lambda x: np.ascontiguousarray(x[:, a:b][None])
+        os_, ls_ = attention_fwd(sl(q), sl(k), sl(v), scale, causal, nthreads)
+        o[:, a:b], lse[:, a:b] = os_[0], ls_[0]
+    return o, lse
+
+
+def attention_bwd_varlen(q, k, v, do, cu_seqlens, scale, causal, nthreads=0):
+    """dQ, dK, dV [H,T,d] of a packed batch (see attention_fwd_varlen)."""
+    H, T, d = q.shape
+    dq, dk, dv = (np.full((H, T, d), np.nan) for _ in range(3))
+    for a, b in _sequences(cu_seqlens):
+        if b == a:
+            continue
+        sl = lambda x: np.ascontiguousarray(x[:, a:b][None])
+        g = attention_bwd(sl(q), sl(k), sl(v), sl(do), scale, causal, None, nthreads)
+        dq[:, a:b], dk[:, a:b], dv[:, a:b] = g[0][0], g[1][0], g[2][0]
+    return dq, dk, dv

@@ -281,3 +281,61 @@ def test_ragged_tile_counts_by_hand():
     # query tile 0: key tiles 0,1 masked (cross the diagonal), 2,3 skipped;
     # query tile 1: key tiles 0,1 full, 2,3 masked
     assert oracle.tile_counts(256, True, 128, 64) == (2, 4, 2)
+
+
+# ---------------------------------------------------------------- packed variable-length batches
+
+def _packed(seed, lens, H=2, d=16):
+    rng = np.random.default_rng(seed)
+    T = sum(lens)
+    q, k, v, do = (rng.standard_normal((H, T, d)) for _ in range(4))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    return q, k, v, do, cu
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_equal_lengths_is_the_dense_batch(causal):
+    """B sequences of one length N packed head-major are the dense [B,H,N,d]
+    batch with the batch and head axes swapped."""
+    B, H, N, d = 3, 2, 37, 16
+    q, k, v, do, cu = _packed(11, [N] * B, H, d)
+    dense = lambda x: np.ascontiguousarray(x.reshape(H, B, N, d).transpose(1, 0, 2, 3))
+    o, lse = oracle.attention_fwd_varlen(q, k, v, cu, 0.3, causal)
+    o_d, lse_d = oracle.attention_fwd(dense(q), dense(k), dense(v), 0.3, causal)
+    np.testing.assert_array_equal(o.reshape(H, B, N, d).transpose(1, 0, 2, 3), o_d)
+    np.testing.assert_array_equal(lse.reshape(H, B, N).transpose(1, 0, 2), lse_d)
+    g = oracle.attention_bwd_varlen(q, k, v, do, cu, 0.3, causal)
+    g_d = oracle.attention_bwd(dense(q), dense(k), dense(v), dense(do), 0.3, causal)
+    for a, b in zip(g, g_d):
+        np.testing.assert_array_equal(a.reshape(H, B, N, d).transpose(1, 0, 2, 3), b)
+
+
+def test_varlen_sequences_do_not_see_each_other():
+    """Changing one sequence's keys and values leaves every other sequence's
+    output and gradients unchanged, and changes its own."""
+    lens = [5, 0, 17, 1, 9]
+    q, k, v, do, cu = _packed(12, lens)
+    o, lse = oracle.attention_fwd_varlen(q, k, v, cu, 0.25, True)
+    g = oracle.attention_bwd_varlen(q, k, v, do, cu, 0.25, True)
+    k2, v2 = k.copy(), v.copy()
+    a, b = cu[2], cu[3]
+    k2[:, a:b] += 1.0
+    v2[:, a:b] *= -2.0
+    o2, lse2 = oracle.attention_fwd_varlen(q, k2, v2, cu, 0.25, True)
+    g2 = oracle.attention_bwd_varlen(q, k2, v2, do, cu, 0.25, True)
+    outside = np.r_[0:a, b:cu[-1]]
+    np.testing.assert_array_equal(o2[:, outside], o[:, outside])
+    np.testing.assert_array_equal(lse2[:, outside], lse[:, outside])
+    for x, y in zip(g, g2):
+        np.testing.assert_array_equal(x[:, outside], y[:, outside])
+    assert np.abs(o2[:, a:b] - o[:, a:b]).max() > 1e-3
+
+
+def test_varlen_length_one_sequence_returns_its_value_row():
+    """A sequence of one token attends only to itself: O = V, LSE = the scaled
+    self-score (page "tm_flash_attention_math", "The problem": the single-query
+    definition with one key)."""
+    q, k, v, do, cu = _packed(13, [4, 1, 3])
+    o, lse = oracle.attention_fwd_varlen(q, k, v, cu, 0.5, False)
+    np.testing.assert_allclose(o[:, 4], v[:, 4], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse[:, 4], 0.5 * np.einsum("hd,hd->h", q[:, 4], k[:, 4]), atol=1e-14)

@@ -32,7 +32,9 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from online_softmax_08_gb300.inputs import HEADLINE, WORKLOADS, default_scale, make_inputs  # noqa: E402
+from online_softmax_08_gb300.inputs import (HEADLINE, VARLEN_WORKLOADS, WORKLOADS,  # noqa: E402
+                                            default_scale, make_inputs, make_varlen_inputs,
+                                            varlen_lengths)
 
 METRIC = "attention fwd/bwd TFLOP/s, N=8192 d=128 bf16 causal; % of GB300 BF16 peak"
 UNIT = "TFLOP/s"
@@ -407,13 +409,95 @@ def run_gpu(args):
     return 0
 
 
+def run_gpu_varlen(args):
+    """Profiling mode for a packed variable-length workload (one GPU): one step is
+    fattn_fwd_varlen then fattn_bwd_varlen on all sequences."""
+    from online_softmax_08_gb300 import fattn
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    w = VARLEN_WORKLOADS[args.workload]
+    H, d, causal = w["H"], w["d"], w["causal"]
+    lens = varlen_lengths(w["B"], w["lo"], w["hi"], w["seed"])
+    q, k, v, do, cu = (x.to(device) for x in make_varlen_inputs(lens, H, d, w["seed"], True))
+    T, mx, B = int(sum(lens)), max(lens), len(lens)
+    scale = default_scale(d)
+    f_fwd = sum(4.0 * H * n * n * d * (0.5 if causal else 1.0) for n in lens)
+    f_bwd = 2.5 * f_fwd
+    o = torch.empty_like(q)
+    lse = torch.empty((H, T), dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fattn.fattn_bwd_workspace_bytes(1, H, T, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    K = args.steps
+    evs = [[ev() for _ in range(3)] for _ in range(K)]
+
+    def step(i=None):
+        if i is not None:
+            evs[i][0].record(stream)
+        fattn.fattn_fwd_varlen(q, k, v, o, lse, cu, B, H, mx, T, d, scale, causal, stream)
+        if i is not None:
+            evs[i][1].record(stream)
+        fattn.fattn_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, cu, B, H, mx, T, d, scale, causal,
+                               ws, ws_bytes, stream)
+        if i is not None:
+            evs[i][2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    for e3 in evs:
+        for e in e3:
+            e.record(stream)
+    torch.cuda.synchronize(device)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(device)
+    t0, t1 = ev(), ev()
+    t0.record(stream)
+    for i in range(K):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    clk = clocks.stop()
+    assert fattn.fattn_device_error() == 0, "an in-kernel wait timed out"
+    ms = t0.elapsed_time(t1) / K
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    peak_tf, _, peak_src = peaks()
+    fwd_tf, bwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12, f_bwd / (bwd_ms * 1e-3) / 1e12
+    line = {
+        "metric": "attention fwd/bwd TFLOP/s, packed variable-length batch, d=%d bf16%s"
+                  % (d, " causal" if causal else ""),
+        "value": (f_fwd + f_bwd) / (ms * 1e-3) / 1e12, "unit": UNIT, "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "H": H, "d": d, "causal": causal,
+                   "lengths": "uniform [%d, %d], seed %d" % (w["lo"], w["hi"], w["seed"]),
+                   "total_rows": T, "max_seqlen": mx,
+                   "l2": "inputs larger than L2 (Q, K, V, dO: %.0f MB each)" % (H * T * d * 2 / 1e6)},
+        "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peak_tf},
+        "bwd": {"ms": bwd_ms, "tflops": bwd_tf, "frac_of_peak": bwd_tf / peak_tf},
+        "roofline": {"kernel": "fattn_bwd_kernel<%d> (varlen)" % d, "bound": "tensor",
+                     "achieved": bwd_tf, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": bwd_tf / peak_tf, "peak_source": peak_src + " (bf16 burst)",
+                     "traffic": None},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": 4 * K, "clocks": clk,
+    }
+    print(json.dumps(_clean(line)), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS),
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS) + sorted(VARLEN_WORKLOADS),
                     help="profiling only: the benchmark's workload is the default")
     ap.add_argument("--pass", dest="passes", default="both", choices=["both", "fwd", "bwd"],
                     help="profiling only: time one pass; a benchmark step is both")
@@ -423,6 +507,8 @@ def main(argv=None):
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload in VARLEN_WORKLOADS:
+        return run_gpu_varlen(args)
     return run_gpu(args)
 
 

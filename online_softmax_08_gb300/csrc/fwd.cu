@@ -81,9 +81,13 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_qb = (p.N + 255) / 256;  // p.N: the (longest) sequence length
   // heaviest (last) query blocks first
+  // dense: query-block-major, so the CTAs in flight cover every (b, h); varlen:
+  // one (sequence, head) unit after another, so the CTAs in flight share their
+  // unit's K/V in L2 (a unit-spread order streams each CTA's K/V from DRAM)
   const int units = VARLEN ? p.vl.B * p.vl.H : p.BH;
-  const int qb = n_qb - 1 - (int)(blockIdx.x / (unsigned)units);
-  const int unit = (int)(blockIdx.x % (unsigned)units);
+  const int qb = VARLEN ? n_qb - 1 - (int)(blockIdx.x % (unsigned)n_qb)
+                        : n_qb - 1 - (int)(blockIdx.x / (unsigned)units);
+  const int unit = VARLEN ? (int)(blockIdx.x / (unsigned)n_qb) : (int)(blockIdx.x % (unsigned)units);
   SeqView seq;
   if constexpr (VARLEN) {
     if (!seq_view(p.vl, p.N, unit / p.vl.H, unit % p.vl.H, unit, p.N, &seq)) {

@@ -97,3 +97,11 @@ def varlen_lengths(B, lo, hi, seed):
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
     return torch.randint(lo, hi + 1, (B,), generator=g).tolist()
+
+
+# Packed variable-length workloads (profiling; not one of the fixed-shape
+# workloads above): B sequences with lengths drawn uniformly from [lo, hi].
+VARLEN_WORKLOADS = {
+    "varlen_b16h16_len512to8192_d128_causal": dict(B=16, H=16, d=128, lo=512, hi=8192,
+                                                   seed=1241, causal=True),
+}

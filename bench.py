@@ -32,9 +32,9 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from online_softmax_08_gb300.inputs import (HEADLINE, VARLEN_WORKLOADS, WORKLOADS,  # noqa: E402
-                                            default_scale, make_inputs, make_varlen_inputs,
-                                            varlen_lengths)
+from online_softmax_08_gb300.inputs import (DECODE_WORKLOADS, HEADLINE,  # noqa: E402
+                                            VARLEN_WORKLOADS, WORKLOADS, default_scale,
+                                            make_inputs, make_varlen_inputs, varlen_lengths)
 
 METRIC = "attention fwd/bwd TFLOP/s, N=8192 d=128 bf16 causal; % of GB300 BF16 peak"
 UNIT = "TFLOP/s"
@@ -491,16 +491,78 @@ def run_gpu_varlen(args):
     return 0
 
 
+def run_gpu_decode(args):
+    """Profiling mode for split-KV decoding (one GPU): one step is fattn_decode
+    (split forward + merge).  HBM-bound: the roofline is the bytes of K and V
+    read once (plus Q, O, LSE) against the measured copy bandwidth."""
+    from online_softmax_08_gb300 import fattn
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    w = DECODE_WORKLOADS[args.workload]
+    B, H, Nq, Nkv, d, causal = w["B"], w["H"], w["Nq"], w["Nkv"], w["d"], w["causal"]
+    q, k, v = make_inputs(B, H, Nkv, d, w["seed"])
+    q = q[:, :, Nkv - Nq:].contiguous()
+    q, k, v = q.to(device), k.to(device), v.to(device)
+    scale = default_scale(d)
+    lib = fattn.load()
+    n_splits = int(args.splits)
+    S = lib.fattn_decode_splits(B, H, Nq, Nkv, d, n_splits)
+    ws = torch.empty(int(lib.fattn_decode_workspace_bytes(B, H, Nq, Nkv, d, n_splits)),
+                     dtype=torch.uint8, device=device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    step = lambda: fattn.decode(q, k, v, scale, causal, n_splits, ws, stream)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    K = args.steps
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(K):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    clk = clocks.stop()
+    assert fattn.fattn_device_error() == 0, "an in-kernel wait timed out"
+    ms = t0.elapsed_time(t1) / K
+    nbytes = (2 * B * H * Nkv * d + 2 * B * H * Nq * d) * 2 + B * H * Nq * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    _, peak_hbm, peak_src = peaks()
+    line = {
+        "metric": "split-KV decode GB/s (K, V read once), d=%d bf16" % d,
+        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "H": H, "Nq": Nq, "Nkv": Nkv, "d": d,
+                   "causal": causal, "n_splits": S,
+                   "l2": "inputs larger than L2 (K, V: %.0f MB each)" % (B * H * Nkv * d * 2 / 1e6)},
+        "roofline": {"kernel": "fattn_fwd_kernel<%d> (split) + merge_kernel" % d, "bound": "hbm",
+                     "achieved": gbs, "peak": peak_hbm, "unit": "GB/s", "frac": gbs / peak_hbm,
+                     "peak_source": peak_src + " (copy)", "traffic": None,
+                     "algorithmic_bytes": nbytes},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": 2 * K, "clocks": clk,
+    }
+    print(json.dumps(_clean(line)), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS) + sorted(VARLEN_WORKLOADS),
+    ap.add_argument("--workload", default=HEADLINE,
+                    choices=sorted(WORKLOADS) + sorted(VARLEN_WORKLOADS) + sorted(DECODE_WORKLOADS),
                     help="profiling only: the benchmark's workload is the default")
     ap.add_argument("--pass", dest="passes", default="both", choices=["both", "fwd", "bwd"],
                     help="profiling only: time one pass; a benchmark step is both")
+    ap.add_argument("--splits", default=0, help="decode workloads: key ranges (0 = automatic)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -509,6 +571,8 @@ def main(argv=None):
         return run_reference(args)
     if args.workload in VARLEN_WORKLOADS:
         return run_gpu_varlen(args)
+    if args.workload in DECODE_WORKLOADS:
+        return run_gpu_decode(args)
     return run_gpu(args)
 
 

@@ -132,6 +132,43 @@ int fattn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
                      float scale, int causal, void* workspace, size_t workspace_bytes,
                      void* stream);
 
+/* Split-KV attention for a few queries against many keys (decoding).
+ * q [B,H,Nq,d], k, v [B,H,Nkv,d] bf16, 1 <= Nq <= Nkv; outputs o [B,H,Nq,d]
+ * bf16 and lse [B,H,Nq] fp32, all DEVICE pointers, 16-byte aligned.  The
+ * queries are the LAST Nq positions of the sequence: with causal, query i
+ * sees keys j <= Nkv - Nq + i (Nq == Nkv is fattn_fwd's causal mask).
+ * The 128-key tiles are cut into key ranges, one per CTA of the forward
+ * kernel, each leaving its range's normalised result and log-sum-exp in the
+ * workspace; a merge kernel combines them (fattn_merge_partials).  This is
+ * the block-wise recurrence of "tm_flash_attention_math" ("The block-wise
+ * update, and the full algorithm"), with whole blocks' states merged, which
+ * the page's "Proof of exactness" allows in any order.
+ * n_splits: 0 = automatic (about ten waves of CTAs, at least four tiles per
+ * range), else the requested number
+ * of ranges (capped at one per tile; the count used is fattn_decode_splits).
+ * workspace: DEVICE memory of fattn_decode_workspace_bytes(...) bytes,
+ * 256-byte aligned, owned by the caller.  Returns FATTN_OK,
+ * FATTN_ERR_INVALID_ARG, FATTN_ERR_UNSUPPORTED, FATTN_ERR_WORKSPACE or
+ * FATTN_ERR_CUDA; launches nothing on an argument error. */
+int fattn_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int Nq, int Nkv, int d, float scale, int causal, int n_splits, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/* Number of key ranges fattn_decode uses for these arguments (0 if invalid). */
+int fattn_decode_splits(int B, int H, int Nq, int Nkv, int d, int n_splits);
+
+/* Workspace bytes fattn_decode needs: S x B*H*Nq x (d + 1) fp32 (0 if invalid). */
+size_t fattn_decode_workspace_bytes(int B, int H, int Nq, int Nkv, int d, int n_splits);
+
+/* Merge of partial results over disjoint key ranges: o_part [S, rows, d] and
+ * lse_part [S, rows] fp32 (range s's normalised output and log-sum-exp; a
+ * range in which a row saw no key has lse = -inf) -> lse = log sum_s
+ * exp(lse_s), o = sum_s exp(lse_s - lse) o_s as bf16 [rows, d]; a row with
+ * every lse_s = -inf gets o = 0 and lse = -inf.  DEVICE pointers, 16-byte
+ * aligned; d in {64, 128}. */
+int fattn_merge_partials(const float* o_part, const float* lse_part, int n_splits, long long rows,
+                         int d, void* o, float* lse, void* stream);
+
 /* Size of the device array that fattn_bwd_noalloc uses as its workspace. */
 #define FATTN_NOALLOC_SCRATCH_BYTES (64u << 20)
 

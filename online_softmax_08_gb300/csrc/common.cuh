@@ -34,6 +34,15 @@ struct FwdParams {
   unsigned int* err;          // device error word
   Varlen vl;
   uint16_t* o;                // O (bf16 bits); varlen writes the last tile of a sequence row by row
+  // Split-KV (decode): N keys, Nq queries aligned to the END of the keys (query
+  // i sits at position N - Nq + i); the key tiles are cut into n_splits ranges
+  // of tiles_per_split tiles, one per CTA, whose normalised partial results go
+  // to o_part [n_splits, BH, Nq, d] and lse_part [n_splits, BH, Nq] (fp32).
+  int Nq;
+  int n_splits;
+  int tiles_per_split;
+  float* o_part;
+  float* lse_part;
 };
 
 struct BwdParams {
@@ -82,6 +91,12 @@ __device__ __forceinline__ bool seq_view(const Varlen& vl, int dense_N, int seq,
 // Launchers (one per translation unit).  Return cudaSuccess or the launch error.
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_fwd_split(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                             const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& p,
+                             cudaStream_t stream);
+// Merge of split partials: lse = log sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s (bf16).
+cudaError_t launch_merge(const float* o_part, const float* lse_part, int n_splits, long long rows,
+                         int d, void* o, float* lse, cudaStream_t stream);
 
 cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* delta, float* dq_acc,
                                   long long rows, int d, cudaStream_t stream);

@@ -64,8 +64,10 @@ enum {
 };
 
 // VARLEN: the CTA's sequence comes from p.vl.cu_seqlens (packed head-major
-// rows); otherwise the dense [B, H, N, d] layout.
-template <int D, bool VARLEN>
+// rows); otherwise the dense [B, H, N, d] layout.  SPLIT (dense only): the CTA
+// covers one range of key tiles and writes its normalised partial O and LSE
+// (fp32) for the merge kernel; queries are the last p.Nq positions.
+template <int D, bool VARLEN, bool SPLIT>
 __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
     fattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -79,15 +81,18 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
   uint8_t* smem = smem_raw + (sbase - raw);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_qb = (p.N + 255) / 256;  // p.N: the (longest) sequence length
+  // SPLIT: blockIdx = (query block, unit, split) with the split fastest
+  const int split = SPLIT ? (int)(blockIdx.x % (unsigned)p.n_splits) : 0;
+  const unsigned bidx = SPLIT ? blockIdx.x / (unsigned)p.n_splits : blockIdx.x;
+  const int n_qb = ((SPLIT ? p.Nq : p.N) + 255) / 256;  // p.N: the (longest) sequence length
   // heaviest (last) query blocks first
   // dense: query-block-major, so the CTAs in flight cover every (b, h); varlen:
   // one (sequence, head) unit after another, so the CTAs in flight share their
   // unit's K/V in L2 (a unit-spread order streams each CTA's K/V from DRAM)
   const int units = VARLEN ? p.vl.B * p.vl.H : p.BH;
-  const int qb = VARLEN ? n_qb - 1 - (int)(blockIdx.x % (unsigned)n_qb)
-                        : n_qb - 1 - (int)(blockIdx.x / (unsigned)units);
-  const int unit = VARLEN ? (int)(blockIdx.x / (unsigned)n_qb) : (int)(blockIdx.x % (unsigned)units);
+  const int qb = VARLEN ? n_qb - 1 - (int)(bidx % (unsigned)n_qb)
+                        : n_qb - 1 - (int)(bidx / (unsigned)units);
+  const int unit = VARLEN ? (int)(bidx / (unsigned)n_qb) : (int)(bidx % (unsigned)units);
   SeqView seq;
   if constexpr (VARLEN) {
     if (!seq_view(p.vl, p.N, unit / p.vl.H, unit % p.vl.H, unit, p.N, &seq)) {
@@ -98,16 +103,21 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
   } else {
     seq = SeqView{p.N, 0, unit, (long long)unit * p.N};
   }
-  const int N = seq.N;
+  const int N = seq.N;         // keys
+  const int Nq = SPLIT ? p.Nq : N;  // queries
+  const int off = N - Nq;      // query i sits at key position i + off (0 unless SPLIT)
   const int bh = seq.z;        // TMA z coordinate
   const int row0 = seq.row0;   // first row of the sequence in the tensor
   const int n_kv_total = (N + C::BN - 1) / C::BN;
+  // key tiles [jlo, jhi) belong to this CTA (all of them unless SPLIT)
+  const int jlo = SPLIT ? split * p.tiles_per_split : 0;
+  const int jhi = SPLIT ? jlo + p.tiles_per_split : 0x7fffffff;
 
-  // rows [r0_s, r0_s + 128) of subtile s see key tiles [0, nt_s)
+  // rows [r0_s, r0_s + 128) of subtile s see key tiles [jlo, jlo + nt_s)
   auto tiles_for = [&](int r0) {
-    if (r0 >= N) return 0;
-    const int last_key = p.causal ? min(r0 + C::BM - 1, N - 1) : N - 1;
-    return last_key / C::BN + 1;
+    if (r0 >= Nq) return 0;
+    const int last_key = p.causal ? min(r0 + C::BM - 1 + off, N - 1) : N - 1;
+    return max(0, min(last_key / C::BN + 1, jhi) - jlo);
   };
   const int r0_0 = qb * 256, r0_1 = qb * 256 + 128;
   const int nt0 = tiles_for(r0_0), nt1 = tiles_for(r0_1);
@@ -172,8 +182,8 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
         const CUtensorMap* m = (i & 1) ? &tm_v : &tm_k;
         mbar_arrive_expect_tx(kv_full0 + 8u * slot, C::TILE);
         for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(dst + h * C::HALF, m, kv_full0 + 8u * slot, h * 64, row0 + (i >> 1) * C::BN,
-                      bh);
+          tma_load_3d(dst + h * C::HALF, m, kv_full0 + 8u * slot, h * 64,
+                      row0 + (jlo + (i >> 1)) * C::BN, bh);
         issued = i + 1;
       }
       // drain: at most one load per slot can still be landing, the latest one
@@ -278,12 +288,12 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
         for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(u[c][i]);
 
       // masks go in before the block maximum
-      const int c0 = j * C::BN;
+      const int c0 = (jlo + j) * C::BN;
       const bool need_mask =
-          (p.causal && min(c0 + C::BN - 1, N - 1) > my_r0) || (c0 + C::BN > N);
+          (p.causal && min(c0 + C::BN - 1, N - 1) > my_r0 + off) || (c0 + C::BN > N);
       if (need_mask) {
         int lim = N - c0;
-        if (p.causal) lim = min(lim, row - c0 + 1);
+        if (p.causal) lim = min(lim, row + off - c0 + 1);
 #pragma unroll
         for (int k = 0; k < 128; ++k)
           if (k >= lim) sv[k] = -INFINITY;
@@ -350,7 +360,38 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
       mbar_arrive(bar(B_P_FULL + s));
     }
 
-    if (my_nt > 0) {
+    if (SPLIT && my_r0 < Nq) {
+      // ------------------------------------------------------------ split epilogue:
+      // normalised partial O (fp32) and partial LSE of this key range; a row that
+      // saw no key here gets O = 0 and LSE = -inf, which the merge weighs by zero
+      const size_t prow = ((size_t)split * p.BH + bh) * Nq + row;
+      const bool has = l_run > 0.f;
+      const float inv_l = has ? 1.f / l_run : 0.f;
+      if (my_nt > 0) {
+        mbar_wait(bar(B_PV_DONE + s), (my_nt - 1) & 1, wctx, ERR_SITE_FWD | 0x24);
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);  // warp-wide: every lane loads, valid rows store
+          tmem_wait_ld(o);
+          if (row < Nq) {
+            float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D + c * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              dst[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv_l,
+                                    __uint_as_float(o[4 * q4 + 1]) * inv_l,
+                                    __uint_as_float(o[4 * q4 + 2]) * inv_l,
+                                    __uint_as_float(o[4 * q4 + 3]) * inv_l);
+          }
+        }
+      } else if (row < Nq) {
+        float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
+#pragma unroll
+        for (int q4 = 0; q4 < D / 4; ++q4) dst[q4] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (row < Nq) p.lse_part[prow] = has ? (m_run * sl2 + lg2(l_run)) * kLn2 : -INFINITY;
+    } else if (!SPLIT && my_nt > 0) {
       // ------------------------------------------------------------ epilogue
       mbar_wait(bar(B_PV_DONE + s), (my_nt - 1) & 1, wctx, ERR_SITE_FWD | 0x23);
       tc_fence_after();
@@ -416,19 +457,22 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
   }
 }
 
-template <int D, bool VARLEN>
+template <int D, bool VARLEN, bool SPLIT>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                    const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
   using C = Fwd<D>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(fattn_fwd_kernel<D, VARLEN>,
+  static_assert(!(VARLEN && SPLIT), "split-KV is dense only");
+  cudaError_t e = cudaFuncSetAttribute(fattn_fwd_kernel<D, VARLEN, SPLIT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const long long n_qb = (p.N + 255) / 256;
-  const long long blocks = n_qb * (VARLEN ? (long long)p.vl.B * p.vl.H : p.BH);
+  const long long n_qb = ((SPLIT ? p.Nq : p.N) + 255) / 256;
+  const long long blocks = n_qb * (VARLEN ? (long long)p.vl.B * p.vl.H : p.BH) *
+                           (SPLIT ? p.n_splits : 1);
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (blocks == 0) return cudaSuccess;
-  fattn_fwd_kernel<D, VARLEN><<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, to, p);
+  fattn_fwd_kernel<D, VARLEN, SPLIT><<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv,
+                                                                                        to, p);
   return cudaGetLastError();
 }
 
@@ -437,10 +481,18 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
   const bool vl = p.vl.cu_seqlens != nullptr;
-  if (d == 128) return vl ? launch<128, true>(tq, tk, tv, to, p, stream)
-                          : launch<128, false>(tq, tk, tv, to, p, stream);
-  if (d == 64) return vl ? launch<64, true>(tq, tk, tv, to, p, stream)
-                         : launch<64, false>(tq, tk, tv, to, p, stream);
+  if (d == 128) return vl ? launch<128, true, false>(tq, tk, tv, to, p, stream)
+                          : launch<128, false, false>(tq, tk, tv, to, p, stream);
+  if (d == 64) return vl ? launch<64, true, false>(tq, tk, tv, to, p, stream)
+                         : launch<64, false, false>(tq, tk, tv, to, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd_split(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                             const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& p,
+                             cudaStream_t stream) {
+  if (d == 128) return launch<128, false, true>(tq, tk, tv, to, p, stream);
+  if (d == 64) return launch<64, false, true>(tq, tk, tv, to, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -37,6 +37,10 @@ SIGNATURES = {
     "fattn_tile_sizes": (_i, [_i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "fattn_device_error": (_i, [ctypes.POINTER(ctypes.c_uint), _i]),
     "fattn_check_wait_timeout": (_i, [_vp]),
+    "fattn_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz, _vp]),
+    "fattn_decode_splits": (_i, [_i, _i, _i, _i, _i, _i]),
+    "fattn_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "fattn_merge_partials": (_i, [_vp, _vp, _i, ctypes.c_longlong, _i, _vp, _vp, _vp]),
     "fattn_fwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "fattn_bwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
                               _i, _f, _i, _vp, _sz, _vp]),
@@ -236,3 +240,31 @@ def backward_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen, scale, causal, 
     fattn_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, cu_seqlens, B, H, max_seqlen, T, d, scale,
                      causal, workspace, workspace.numel() * workspace.element_size(), stream)
     return dq, dk, dv
+
+
+def decode(q, k, v, scale, causal, n_splits=0, workspace=None, stream=None):
+    """O, LSE of few queries q [B,H,Nq,d] against k, v [B,H,Nkv,d] (the queries
+    are the last Nq positions) by split-KV plus merge."""
+    B, H, Nq, d = _shape(q)
+    Nkv = k.shape[2]
+    lib = load()
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    nbytes = int(lib.fattn_decode_workspace_bytes(B, H, Nq, Nkv, d, n_splits))
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    _check("fattn_decode", lib.fattn_decode(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nkv, d, float(scale),
+        int(bool(causal)), int(n_splits), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return o, lse
+
+
+def merge_partials(o_part, lse_part, stream=None):
+    """Merge fp32 partials o_part [S, rows, d], lse_part [S, rows] -> bf16 o [rows, d], lse."""
+    S, rows, d = o_part.shape
+    o = torch.empty((rows, d), dtype=torch.bfloat16, device=o_part.device)
+    lse = torch.empty((rows,), dtype=torch.float32, device=o_part.device)
+    _check("fattn_merge_partials", load().fattn_merge_partials(
+        _ptr(o_part), _ptr(lse_part), S, rows, d, _ptr(o), _ptr(lse), _stream(stream)))
+    return o, lse

@@ -105,3 +105,10 @@ VARLEN_WORKLOADS = {
     "varlen_b16h16_len512to8192_d128_causal": dict(B=16, H=16, d=128, lo=512, hi=8192,
                                                    seed=1241, causal=True),
 }
+
+
+# Decoding workloads (profiling): Nq queries at the end of Nkv keys, Q, K, V ~ N(0, 1).
+DECODE_WORKLOADS = {
+    "decode_b4h32_nq1_nkv32768_d128": dict(B=4, H=32, Nq=1, Nkv=32768, d=128, seed=1242,
+                                           causal=True),
+}

@@ -14,6 +14,10 @@ compiles it on demand with gcc and marshals numpy arrays through ctypes.
   attention_fwd_varlen, attention_bwd_varlen
                       -- packed variable-length batches: each sequence is its own
                          attention problem (the definition applied per sequence)
+  attention_fwd_decode
+                      -- few queries at the end of a long sequence (numpy, fp64)
+  merge_partials      -- block states (o_s, lse_s) over disjoint key ranges
+                         merged by the block-wise update (numpy, fp64)
 
 Inputs are numpy float64 arrays of shape [B, H, N, d] (contiguous).
 """
@@ -183,3 +187,55 @@ def attention_bwd_varlen(q, k, v, do, cu_seqlens, scale, causal, nthreads=0):
         g = attention_bwd(sl(q), sl(k), sl(v), sl(do), scale, causal, None, nthreads)
         dq[:, a:b], dk[:, a:b], dv[:, a:b] = g[0][0], g[1][0], g[2][0]
     return dq, dk, dv
+
+
+def attention_fwd_decode(q, k, v, scale, causal):
+    """O [B,H,Nq,d], LSE [B,H,Nq] for queries that are the LAST Nq positions of a
+    sequence of Nkv keys: query i sits at position Nkv - Nq + i and, with
+    causal, sees keys j <= Nkv - Nq + i.  The definition written out in numpy
+    fp64: S = scale Q K^T, the mask, the three-pass safe softmax of page
+    "tm_flash_attention_math" ("Safe softmax"), O = P V, LSE = m + ln l."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    B, H, Nq, d = q.shape
+    Nkv = k.shape[2]
+    s = scale * np.einsum("bhid,bhjd->bhij", q, k)
+    if causal:
+        pos = np.arange(Nq)[:, None] + (Nkv - Nq)
+        s = np.where(np.arange(Nkv)[None, :] <= pos, s, -np.inf)
+    m = s.max(axis=-1, keepdims=True)                    # pass 1
+    e = np.exp(s - m)
+    l = e.sum(axis=-1, keepdims=True)                    # pass 2
+    p = e / l                                            # pass 3
+    return np.einsum("bhij,bhjd->bhid", p, v), (m + np.log(l))[..., 0]
+
+
+def merge_partials(o_part, lse_part):
+    """Merge S block states over disjoint key ranges, taken in order s = 0, 1, ...
+    with the block-wise update of page "tm_flash_attention_math" ("The
+    block-wise update, and the full algorithm"): a block with log-sum-exp
+    lse_s and normalised output o_s carries m_s = lse_s, l_s = 1, o~_s = o_s;
+    m_new = max(m, m_s), alpha = exp(m - m_new), l = alpha l + exp(m_s - m_new),
+    o~ = alpha o~ + exp(m_s - m_new) o_s; finally o = o~ / l, lse = m + ln l.
+    A block with lse_s = -inf (no visible key) leaves the state unchanged.
+    o_part [S, rows, d], lse_part [S, rows] -> o [rows, d], lse [rows]."""
+    o_part = np.asarray(o_part, dtype=np.float64)
+    lse_part = np.asarray(lse_part, dtype=np.float64)
+    S, rows, d = o_part.shape
+    o = np.zeros((rows, d))
+    lse = np.full(rows, -np.inf)
+    for r in range(rows):
+        m, l, ot = -np.inf, 0.0, np.zeros(d)
+        for s_ in range(S):
+            ms = lse_part[s_, r]
+            if ms == -np.inf:
+                continue
+            m_new = max(m, ms)
+            alpha = np.exp(m - m_new) if m != -np.inf else 0.0
+            w = np.exp(ms - m_new)
+            l = alpha * l + w
+            ot = alpha * ot + w * o_part[s_, r]
+            m = m_new
+        if l > 0.0:
+            o[r] = ot / l
+            lse[r] = m + np.log(l)
+    return o, lse

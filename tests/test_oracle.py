@@ -339,3 +339,66 @@ def test_varlen_length_one_sequence_returns_its_value_row():
     o, lse = oracle.attention_fwd_varlen(q, k, v, cu, 0.5, False)
     np.testing.assert_allclose(o[:, 4], v[:, 4], rtol=0, atol=1e-15)
     np.testing.assert_allclose(lse[:, 4], 0.5 * np.einsum("hd,hd->h", q[:, 4], k[:, 4]), atol=1e-14)
+
+
+# ---------------------------------------------------------------- decoding and block-state merge
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_decode_rows_are_the_last_rows_of_full_attention(causal):
+    """Queries at the end of a sequence: the decode oracle's rows equal the last
+    Nq rows of the dense oracle run on the whole sequence (the C three-pass
+    oracle; the decode oracle is numpy)."""
+    rng = np.random.default_rng(21)
+    B, H, Nkv, Nq, d = 2, 2, 57, 5, 16
+    k, v = rng.standard_normal((B, H, Nkv, d)), rng.standard_normal((B, H, Nkv, d))
+    q_full = rng.standard_normal((B, H, Nkv, d))
+    o_full, lse_full = oracle.attention_fwd(q_full, k, v, 0.3, causal)
+    o, lse = oracle.attention_fwd_decode(q_full[:, :, -Nq:], k, v, 0.3, causal)
+    np.testing.assert_allclose(o, o_full[:, :, -Nq:], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse, lse_full[:, :, -Nq:], rtol=1e-12, atol=1e-13)
+
+
+def test_decode_single_query_sees_every_key_when_causal():
+    rng = np.random.default_rng(22)
+    q, k, v = rng.standard_normal((1, 3, 1, 8)), rng.standard_normal((1, 3, 40, 8)), rng.standard_normal((1, 3, 40, 8))
+    a = oracle.attention_fwd_decode(q, k, v, 0.5, True)
+    b = oracle.attention_fwd_decode(q, k, v, 0.5, False)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def _range_states(q, k, v, scale, bounds):
+    """Per key range [a, b): that range's normalised output and log-sum-exp."""
+    os_, ls_ = [], []
+    for a, b in bounds:
+        o, lse = oracle.attention_fwd_decode(q, k[:, :, a:b], v[:, :, a:b], scale, False)
+        os_.append(o.reshape(-1, q.shape[-1]))
+        ls_.append(lse.reshape(-1))
+    return np.stack(os_), np.stack(ls_)
+
+
+@pytest.mark.parametrize("bounds", [[(0, 10), (10, 57)], [(0, 1), (1, 2), (2, 30), (30, 57)],
+                                    [(30, 57), (0, 30)]])
+def test_merged_key_ranges_give_full_attention(bounds):
+    """Exactness of the block-wise update ("Proof of exactness"): merging the
+    states of disjoint key ranges, in any order, gives attention over all keys."""
+    rng = np.random.default_rng(23)
+    q, k, v = rng.standard_normal((1, 2, 3, 16)), rng.standard_normal((1, 2, 57, 16)), rng.standard_normal((1, 2, 57, 16))
+    o_ref, lse_ref = oracle.attention_fwd_decode(q, k, v, 0.4, False)
+    o, lse = oracle.merge_partials(*_range_states(q, k, v, 0.4, bounds))
+    np.testing.assert_allclose(o, o_ref.reshape(-1, 16), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse, lse_ref.reshape(-1), rtol=1e-12, atol=1e-13)
+
+
+def test_merge_ignores_ranges_without_visible_keys():
+    rng = np.random.default_rng(24)
+    o_part = rng.standard_normal((3, 4, 8))
+    lse_part = rng.standard_normal((3, 4))
+    lse_part[1] = -np.inf                       # range 1 saw no key for any row
+    o_part[1] = 0.0
+    a = oracle.merge_partials(o_part, lse_part)
+    b = oracle.merge_partials(o_part[[0, 2]], lse_part[[0, 2]])
+    np.testing.assert_allclose(a[0], b[0], rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(a[1], b[1], rtol=1e-14, atol=1e-15)
+    none = oracle.merge_partials(o_part[1:2], lse_part[1:2])
+    assert np.all(none[0] == 0.0) and np.all(none[1] == -np.inf)

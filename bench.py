@@ -33,8 +33,9 @@ if ROOT not in sys.path:
 import torch  # noqa: E402
 
 from online_softmax_08_gb300.inputs import (DECODE_WORKLOADS, HEADLINE,  # noqa: E402
-                                            VARLEN_WORKLOADS, WORKLOADS, default_scale,
-                                            make_inputs, make_varlen_inputs, varlen_lengths)
+                                            SOFTMAX_WORKLOADS, VARLEN_WORKLOADS, WORKLOADS,
+                                            default_scale, make_inputs, make_softmax_input,
+                                            make_varlen_inputs, varlen_lengths)
 
 METRIC = "attention fwd/bwd TFLOP/s, N=8192 d=128 bf16 causal; % of GB300 BF16 peak"
 UNIT = "TFLOP/s"
@@ -551,6 +552,57 @@ def run_gpu_decode(args):
     return 0
 
 
+def run_gpu_softmax(args):
+    """Profiling mode for the row softmax (one GPU): HBM-bound, one read and one
+    write of every element (rows fit the shared-memory staging)."""
+    from online_softmax_08_gb300 import fattn
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    w = SOFTMAX_WORKLOADS[args.workload]
+    rows, cols = w["rows"], w["cols"]
+    x = make_softmax_input(rows, cols, w["seed"]).to(device)
+    y = torch.empty_like(x)
+    lse = torch.empty((rows,), dtype=torch.float32, device=device)
+    lib = fattn.load()
+    stream = torch.cuda.current_stream(device)
+    step = lambda: fattn._check("fattn_softmax_rows", lib.fattn_softmax_rows(
+        x.data_ptr(), y.data_ptr(), lse.data_ptr(), rows, cols, stream.cuda_stream))
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    K = args.steps
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(K):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / K
+    nbytes = 2 * rows * cols * 4 + rows * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    _, peak_hbm, peak_src = peaks()
+    line = {
+        "metric": "row softmax GB/s (one read, one write per element), fp32",
+        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "rows": rows, "cols": cols,
+                   "l2": "input larger than L2 (%.0f MB)" % (rows * cols * 4 / 1e6)},
+        "roofline": {"kernel": "softmax_rows_kernel", "bound": "hbm", "achieved": gbs,
+                     "peak": peak_hbm, "unit": "GB/s", "frac": gbs / peak_hbm,
+                     "peak_source": peak_src + " (copy)", "traffic": None,
+                     "algorithmic_bytes": nbytes},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": K, "clocks": clk,
+    }
+    print(json.dumps(_clean(line)), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -558,7 +610,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE,
-                    choices=sorted(WORKLOADS) + sorted(VARLEN_WORKLOADS) + sorted(DECODE_WORKLOADS),
+                    choices=sorted(WORKLOADS) + sorted(VARLEN_WORKLOADS) + sorted(DECODE_WORKLOADS)
+                    + sorted(SOFTMAX_WORKLOADS),
                     help="profiling only: the benchmark's workload is the default")
     ap.add_argument("--pass", dest="passes", default="both", choices=["both", "fwd", "bwd"],
                     help="profiling only: time one pass; a benchmark step is both")
@@ -573,6 +626,8 @@ def main(argv=None):
         return run_gpu_varlen(args)
     if args.workload in DECODE_WORKLOADS:
         return run_gpu_decode(args)
+    if args.workload in SOFTMAX_WORKLOADS:
+        return run_gpu_softmax(args)
     return run_gpu(args)
 
 

@@ -169,6 +169,18 @@ size_t fattn_decode_workspace_bytes(int B, int H, int Nq, int Nkv, int d, int n_
 int fattn_merge_partials(const float* o_part, const float* lse_part, int n_splits, long long rows,
                          int d, void* o, float* lse, void* stream);
 
+/* Row-wise softmax with the online normaliser: y[r, :] = exp(x[r, :] - m_r) / l_r
+ * with m_r the row maximum and l_r = sum exp(x[r, :] - m_r), formed in one
+ * sweep by the (m, l) recurrence of "FlashAttention tiles exact softmax
+ * without materializing the score matrix" ("The online softmax recurrence").
+ * x, y: DEVICE fp32 [rows, cols], row-major, 16-byte aligned (y may equal x);
+ * lse: DEVICE fp32 [rows] receiving m_r + ln l_r, or NULL.  A row whose values
+ * are all -inf gets y = 0 and lse = -inf.  Rows of up to 49152 values are read
+ * from HBM once; longer rows twice.  Returns FATTN_OK, FATTN_ERR_INVALID_ARG,
+ * FATTN_ERR_UNSUPPORTED or FATTN_ERR_CUDA. */
+int fattn_softmax_rows(const float* x, float* y, float* lse, long long rows, int cols,
+                       void* stream);
+
 /* Size of the device array that fattn_bwd_noalloc uses as its workspace. */
 #define FATTN_NOALLOC_SCRATCH_BYTES (64u << 20)
 

@@ -22,6 +22,7 @@ struct DeviceInfo {
   bool probed = false;
   bool supported = false;
   unsigned int* err = nullptr;  // device address of g_error_word
+  int n_sm = 0;                 // streaming multiprocessors
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -39,6 +40,8 @@ int current_device(DeviceInfo** out) {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return FATTN_ERR_CUDA;
     info.supported = (major == 10 && minor == 3);
+    if (cudaDeviceGetAttribute(&info.n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FATTN_ERR_CUDA;
     void* addr = nullptr;
     if (cudaGetSymbolAddress(&addr, g_error_word) != cudaSuccess) return FATTN_ERR_CUDA;
     info.err = static_cast<unsigned int*>(addr);
@@ -346,6 +349,20 @@ extern "C" int fattn_merge_partials(const float* o_part, const float* lse_part, 
   const int st = current_device(&dev);
   if (st != FATTN_OK) return st;
   return launch_merge(o_part, lse_part, n_splits, rows, d, o, lse, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? FATTN_OK
+             : FATTN_ERR_CUDA;
+}
+
+extern "C" int fattn_softmax_rows(const float* x, float* y, float* lse, long long rows, int cols,
+                                  void* stream) {
+  if (rows < 1 || cols < 1) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return FATTN_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  const int st = current_device(&dev);
+  if (st != FATTN_OK) return st;
+  return launch_softmax_rows(x, y, lse, rows, cols, dev->n_sm, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? FATTN_OK
              : FATTN_ERR_CUDA;

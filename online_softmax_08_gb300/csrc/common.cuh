@@ -94,6 +94,9 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
 cudaError_t launch_fwd_split(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                              const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& p,
                              cudaStream_t stream);
+// Row-wise softmax with the online normaliser (fp32 in and out, optional LSE per row).
+cudaError_t launch_softmax_rows(const float* x, float* y, float* lse, long long rows, int cols,
+                                int n_sm, cudaStream_t stream);
 // Merge of split partials: lse = log sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s (bf16).
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int n_splits, long long rows,
                          int d, void* o, float* lse, cudaStream_t stream);

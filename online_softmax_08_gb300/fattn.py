@@ -37,6 +37,7 @@ SIGNATURES = {
     "fattn_tile_sizes": (_i, [_i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "fattn_device_error": (_i, [ctypes.POINTER(ctypes.c_uint), _i]),
     "fattn_check_wait_timeout": (_i, [_vp]),
+    "fattn_softmax_rows": (_i, [_vp, _vp, _vp, ctypes.c_longlong, _i, _vp]),
     "fattn_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz, _vp]),
     "fattn_decode_splits": (_i, [_i, _i, _i, _i, _i, _i]),
     "fattn_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
@@ -268,3 +269,13 @@ def merge_partials(o_part, lse_part, stream=None):
     _check("fattn_merge_partials", load().fattn_merge_partials(
         _ptr(o_part), _ptr(lse_part), S, rows, d, _ptr(o), _ptr(lse), _stream(stream)))
     return o, lse
+
+
+def softmax_rows(x, with_lse=False, out=None, stream=None):
+    """Row-wise softmax of a contiguous fp32 [rows, cols] device tensor."""
+    rows, cols = x.shape
+    y = torch.empty_like(x) if out is None else out
+    lse = torch.empty((rows,), dtype=torch.float32, device=x.device) if with_lse else None
+    _check("fattn_softmax_rows", load().fattn_softmax_rows(_ptr(x), _ptr(y), _ptr(lse), rows, cols,
+                                                           _stream(stream)))
+    return (y, lse) if with_lse else y

@@ -112,3 +112,16 @@ DECODE_WORKLOADS = {
     "decode_b4h32_nq1_nkv32768_d128": dict(B=4, H=32, Nq=1, Nkv=32768, d=128, seed=1242,
                                            causal=True),
 }
+
+
+# Row-softmax workloads (profiling): fp32 rows ~ 30 N(0, 1).
+SOFTMAX_WORKLOADS = {
+    "softmax_rows4096_cols32768_f32": dict(rows=4096, cols=32768, seed=1243),
+}
+
+
+def make_softmax_input(rows, cols, seed, scale=30.0):
+    """fp32 CPU tensor [rows, cols] ~ scale * N(0, 1)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return torch.randn((rows, cols), generator=g, dtype=torch.float32) * float(scale)

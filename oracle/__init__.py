@@ -18,6 +18,7 @@ compiles it on demand with gcc and marshals numpy arrays through ctypes.
                       -- few queries at the end of a long sequence (numpy, fp64)
   merge_partials      -- block states (o_s, lse_s) over disjoint key ranges
                          merged by the block-wise update (numpy, fp64)
+  softmax_rows        -- row-wise safe softmax and its log-sum-exp (numpy, fp64)
 
 Inputs are numpy float64 arrays of shape [B, H, N, d] (contiguous).
 """
@@ -239,3 +240,18 @@ def merge_partials(o_part, lse_part):
             o[r] = ot / l
             lse[r] = m + np.log(l)
     return o, lse
+
+
+def softmax_rows(x):
+    """y = softmax of each row of x [rows, cols] and lse = log sum exp per row, by
+    the three passes of page "tm_flash_attention_math" ("Safe softmax"):
+    m = max, l = sum exp(x - m), y = exp(x - m) / l.  A row of only -inf gives
+    y = 0 and lse = -inf (nothing is visible)."""
+    x = np.asarray(x, dtype=np.float64)
+    m = x.max(axis=1, keepdims=True)
+    ok = np.isfinite(m[:, 0])
+    e = np.exp(np.where(ok[:, None], x - np.where(ok[:, None], m, 0.0), -np.inf))
+    l = e.sum(axis=1, keepdims=True)
+    y = np.where(ok[:, None], e / np.where(l > 0, l, 1.0), 0.0)
+    lse = np.where(ok, m[:, 0] + np.log(np.where(l[:, 0] > 0, l[:, 0], 1.0)), -np.inf)
+    return y, lse

@@ -173,3 +173,32 @@ def test_lazy_reference_skips_rescales():
     moves = lambda tr: sum(1 for t in tr[1:] if t["alpha"] != 1.0)
     assert moves(lazy) < moves(exact)
     assert moves(lazy) == 0  # N(0,1) scores never climb 5.5 above the first block's max
+
+
+# ---------------------------------------------------------------- the row softmax oracle
+
+@pytest.mark.parametrize("size", [1, 3, 16, 200])
+def test_row_softmax_is_the_recurrence_with_one_hot_values(size):
+    """With one-hot value vectors (V = I) the recurrence's output is the softmax
+    itself: the row-softmax oracle agrees with the block-wise model for any
+    block size, and its LSE with m + ln l."""
+    rng = np.random.default_rng(700 + size)
+    x = rng.standard_normal(200) * 9.0
+    o, m, l, _ = online_softmax_attention(x.tolist(), np.eye(200).tolist(), blocks_of(200, size))
+    y, lse = oracle.softmax_rows(x[None])
+    np.testing.assert_allclose(y[0], o, rtol=1e-12, atol=1e-15)
+    assert abs(lse[0] - (m + math.log(l))) < 1e-12
+
+
+def test_row_softmax_invariants():
+    rng = np.random.default_rng(701)
+    x = rng.standard_normal((5, 33)) * 20.0
+    y, lse = oracle.softmax_rows(x)
+    np.testing.assert_allclose(y.sum(axis=1), 1.0, rtol=1e-14)
+    y2, lse2 = oracle.softmax_rows(x + 1234.5)               # shift invariance
+    np.testing.assert_allclose(y2, y, rtol=1e-10, atol=1e-15)
+    np.testing.assert_allclose(lse2, lse + 1234.5, rtol=1e-14)
+    np.testing.assert_allclose(y, np.exp(x - lse[:, None]), rtol=1e-12, atol=1e-300)
+    z = np.full((1, 4), -np.inf)
+    yz, lz = oracle.softmax_rows(z)                          # nothing visible
+    assert np.all(yz == 0.0) and lz[0] == -np.inf

@@ -87,3 +87,22 @@ def test_merge_partials_matches_oracle(S, rows, d):
     assert np.array_equal(np.isfinite(_f64(lse)), finite)
     assert np.abs(_f64(lse)[finite] - lse_ref[finite]).max() <= 1e-5
     assert np.all(_f64(o)[1] == 0.0)
+
+
+def test_decode_bench_workload_full():
+    """The benchmark's decoding workload (B4 H32, one query against 32768
+    keys, d128, automatic key ranges), every output row against the oracle."""
+    from online_softmax_08_gb300.inputs import DECODE_WORKLOADS
+    w = DECODE_WORKLOADS["decode_b4h32_nq1_nkv32768_d128"]
+    B, H, Nq, Nkv, d = w["B"], w["H"], w["Nq"], w["Nkv"], w["d"]
+    q, k, v = make_inputs(B, H, Nkv, d, w["seed"])
+    q = q[:, :, Nkv - Nq:].contiguous()
+    dev = torch.device("cuda:0")
+    scale = default_scale(d)
+    o, lse = fattn.decode(q.to(dev), k.to(dev), v.to(dev), scale, w["causal"])
+    torch.cuda.synchronize()
+    assert fattn.fattn_device_error() == 0
+    o_ref, lse_ref = oracle.attention_fwd_decode(_f64(q), _f64(k), _f64(v), scale, w["causal"])
+    err = np.abs(_f64(o) - o_ref)
+    assert err.max() <= O_MAX and err.mean() <= O_MEAN
+    assert np.abs(_f64(lse) - lse_ref).max() <= LSE_MAX

@@ -49,3 +49,20 @@ def test_softmax_rows_in_place():
     torch.cuda.synchronize()
     y_ref, _ = oracle.softmax_rows(x.double().numpy())
     assert np.all(np.abs(xd.double().cpu().numpy() - y_ref) <= 1e-5 * y_ref + 1e-9)
+
+
+def test_softmax_bench_workload_sampled():
+    """The benchmark's workload (4096 rows of 32768 fp32 values), sampled rows
+    against the oracle."""
+    from online_softmax_08_gb300.inputs import SOFTMAX_WORKLOADS, make_softmax_input
+    w = SOFTMAX_WORKLOADS["softmax_rows4096_cols32768_f32"]
+    x = make_softmax_input(w["rows"], w["cols"], w["seed"])
+    dev = torch.device("cuda:0")
+    y, lse = fattn.softmax_rows(x.to(dev), with_lse=True)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([[0, 1, 151, 152, w["rows"] - 1],
+                                     np.random.default_rng(w["seed"]).integers(0, w["rows"], 11)]))
+    y_ref, lse_ref = oracle.softmax_rows(x[rows].double().numpy())
+    yg = y[rows].double().cpu().numpy()
+    assert np.all(np.abs(yg - y_ref) <= 1e-5 * y_ref + 1e-9)
+    assert np.all(np.abs(lse[rows].double().cpu().numpy() - lse_ref) <= 1e-6 * np.abs(lse_ref) + 1e-5)

@@ -102,3 +102,43 @@ def test_bad_offsets_are_reported_not_used():
     torch.cuda.synchronize()
     assert fattn.fattn_device_error() == 0x140
     assert fattn.fattn_device_error() == 0
+
+
+def test_varlen_bench_workload_sampled():
+    """The benchmark's packed workload (16 sequences, lengths uniform in
+    [512, 8192], H16 d128 causal), run as the benchmark runs it: forward rows
+    sampled in every sequence for two heads, each row computed by the oracle
+    one by one; the backward of one head checked in full on the two shortest
+    sequences."""
+    from online_softmax_08_gb300.inputs import VARLEN_WORKLOADS, varlen_lengths
+    w = VARLEN_WORKLOADS["varlen_b16h16_len512to8192_d128_causal"]
+    H, d = w["H"], w["d"]
+    lens = varlen_lengths(w["B"], w["lo"], w["hi"], w["seed"])
+    q, k, v, do, cu = make_varlen_inputs(lens, H, d, w["seed"], with_do=True)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod, cud = (x.to(dev) for x in (q, k, v, do, cu))
+    scale = default_scale(d)
+    o, lse = fattn.forward_varlen(qd, kd, vd, cud, max(lens), scale, True)
+    dq, dk, dv = fattn.backward_varlen(qd, kd, vd, o, lse, dod, cud, max(lens), scale, True)
+    torch.cuda.synchronize()
+    assert fattn.fattn_device_error() == 0
+    of, lf = _f64(o), _f64(lse)
+    rng = np.random.default_rng(w["seed"])
+    cu_np = cu.numpy()
+    for b in range(len(lens)):
+        a, e = int(cu_np[b]), int(cu_np[b + 1])
+        rows = np.unique(np.concatenate([[0, e - a - 1], rng.integers(0, e - a, 6)]))
+        sl = lambda x: _f64(x[:, a:e])[None]
+        heads = np.array([0, H - 1])
+        bh = np.repeat(heads, len(rows))
+        rr = np.tile(rows, len(heads))
+        o_ref, lse_ref = oracle.attention_fwd_rows(sl(q), sl(k), sl(v), scale, True, bh, rr)
+        got = of[bh, a + rr]
+        assert np.abs(got - o_ref).max() <= MAX
+        assert np.abs(lf[bh, a + rr] - lse_ref).max() <= LSE_MAX
+    for b in np.argsort(lens)[:2]:
+        a, e = int(cu_np[b]), int(cu_np[b + 1])
+        sl = lambda x: _f64(x[:, a:e])[None]
+        g_ref = oracle.attention_bwd(sl(q), sl(k), sl(v), sl(do), scale, True, heads=[3])
+        for got, want in zip((dq, dk, dv), g_ref):
+            _close(_f64(got[3:4, a:e]), want)

@@ -8,7 +8,7 @@
 // ("A score tile is temporary state", page "FlashAttention tiles exact
 // softmax without materializing the score matrix").
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads):
 //   warps 0-3  softmax for Q_0, warps 4-7 softmax for Q_1: thread t owns query
 //              row t, which is TMEM lane t, so the row max and row sum need no
 //              shuffles.  They also rescale their O accumulator by alpha when
@@ -18,6 +18,10 @@
 //              loop (so descriptor arithmetic stays warp-uniform) and
 //              elect.sync picks the one lane that issues.
 //   warp 9     one thread issues every TMA load.
+//   warps 10-11 idle: with them the CTA is three whole warpgroups, so setmaxnreg
+//              can move registers from the MMA/TMA warpgroup (48 each) to the
+//              softmax warpgroups (224 each); with the compiler's 168 the
+//              softmax's packed f32x2 arithmetic spilled.
 //
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 after it.
 // P_s (bf16, two per 32-bit column) overwrites the first 64 columns of S_s
@@ -25,6 +29,8 @@
 // so P never touches shared memory.  The MMA thread issues, per subtile,
 // O_s += P_s V_j before S_s = Q_s K_{j+1}^T (the pipe runs them in order).
 // Shared memory: Q_0, Q_1 | K/V ring.
+// setmaxnreg regions may not call functions: inline the wait's slow path
+#define FATTN_INLINE_WAIT_SLOW_PATH
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -34,6 +40,40 @@ namespace {
 constexpr float kLn2 = 0.6931471805599453f;
 // Largest exp2 argument the softmax lets through before it moves its reference.
 constexpr float kRescaleLog2 = 8.f;
+
+
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Two-lane fp32 arithmetic: one instruction for a pair of elements, each lane
+// rounded exactly as the scalar instruction would be.
+// (r0, r1) = (a0, a1) * b + (c, c)
+__device__ __forceinline__ void fma_x2(float a0, float a1, float b, float c, float& r0, float& r1) {
+  asm("{\n\t.reg .b64 a, b, c, r;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %4};\n\t"
+      "mov.b64 c, {%5, %5};\n\t"
+      "fma.rn.f32x2 r, a, b, c;\n\t"
+      "mov.b64 {%0, %1}, r;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (s0, s1) += (a0, a1)
+__device__ __forceinline__ void add_x2(float& s0, float& s1, float a0, float a1) {
+  asm("{\n\t.reg .b64 s, a;\n\t"
+      "mov.b64 s, {%0, %1};\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "add.rn.f32x2 s, s, a;\n\t"
+      "mov.b64 {%0, %1}, s;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
 
 template <int D>
 struct Fwd {
@@ -46,7 +86,10 @@ struct Fwd {
   static constexpr int OFF_KV = OFF_Q + 2 * TILE;
   static constexpr int OFF_BAR = OFF_KV + STAGES * TILE;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers + alignment slack
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 384;  // three warpgroups (warps 10, 11 idle)
+  // registers per thread after setmaxnreg; the launch holds THREADS x REG_LAUNCH
+  static constexpr int REG_LAUNCH = 168, REG_SOFTMAX = 224, REG_CTRL = 48;
+  static_assert((2 * REG_SOFTMAX + REG_CTRL) * 128 <= THREADS * REG_LAUNCH, "register split");
   static constexpr uint32_t TM_S = 0;
   static constexpr uint32_t TM_O = 256;
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, false, false);
@@ -156,7 +199,10 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 9) {
+  if (warp >= 10) {
+    regs_dec<C::REG_CTRL>();  // idle
+  } else if (warp == 9) {
+    regs_dec<C::REG_CTRL>();
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -193,6 +239,7 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 8) {
+    regs_dec<C::REG_CTRL>();
     // ---------------------------------------------------------------- MMA issuer (whole warp)
     {
       auto kv_wait = [&](int i) {
@@ -258,6 +305,7 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax (warps 0-7)
+    regs_inc<C::REG_SOFTMAX>();
     const int s = warp >> 2;
     const int t = threadIdx.x & 127;  // row in the subtile == TMEM lane
     const int my_r0 = s ? r0_1 : r0_0;
@@ -328,14 +376,15 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
 #pragma unroll
         for (int k = 0; k < 64; k += 4) {
           const int kk = h * 64 + k;
-          const float p0 = ex2(fmaf(sv[kk], sl2, -msc));
-          const float p1 = ex2(fmaf(sv[kk + 1], sl2, -msc));
-          const float p2 = ex2(fmaf(sv[kk + 2], sl2, -msc));
-          const float p3 = ex2(fmaf(sv[kk + 3], sl2, -msc));
-          ls0 += p0;
-          ls1 += p1;
-          ls2 += p2;
-          ls3 += p3;
+          float p0, p1, p2, p3;
+          fma_x2(sv[kk], sv[kk + 1], sl2, -msc, p0, p1);
+          fma_x2(sv[kk + 2], sv[kk + 3], sl2, -msc, p2, p3);
+          p0 = ex2(p0);
+          p1 = ex2(p1);
+          p2 = ex2(p2);
+          p3 = ex2(p3);
+          add_x2(ls0, ls1, p0, p1);
+          add_x2(ls2, ls3, p2, p3);
           pk[k / 2] = pack_bf16x2(p0, p1);
           pk[k / 2 + 1] = pack_bf16x2(p2, p3);
         }
@@ -466,6 +515,12 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   cudaError_t e = cudaFuncSetAttribute(fattn_fwd_kernel<D, VARLEN, SPLIT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
+  // the setmaxnreg split hands out at most the launch's registers; with fewer
+  // at launch an increase would never be granted
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, fattn_fwd_kernel<D, VARLEN, SPLIT>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs < C::REG_LAUNCH) return cudaErrorInvalidConfiguration;
   const long long n_qb = ((SPLIT ? p.Nq : p.N) + 255) / 256;
   const long long blocks = n_qb * (VARLEN ? (long long)p.vl.B * p.vl.H : p.BH) *
                            (SPLIT ? p.n_splits : 1);

@@ -1,6 +1,6 @@
 """bench.py's output contract, checked on the CPU through the reference arm
-(the fp64 oracle timed on the host cores): one JSON line with the keys the
-benchmark driver reads, and the reference arm's own markers."""
+(the fp64 oracle timed on the host cores): one JSON line with the keys every
+benchmark line carries, and the reference arm's own markers."""
 import json
 import os
 import subprocess

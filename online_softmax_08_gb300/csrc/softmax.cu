@@ -18,8 +18,8 @@
 namespace fattn {
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kBatch = 8;  // 16-byte loads in flight per thread
+constexpr int kThreads = 1024;
+constexpr int kBatch = 4;  // 16-byte loads in flight per thread (64 KB per CTA)
 constexpr int kSmemCols = 48 * 1024;  // 192 KB of fp32
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -173,7 +173,8 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_kernel(const float* x, 
     // pass 1: the online statistics (staging the row when it fits)
     if (vec) {
       // kBatch independent 16-byte loads per thread before they are consumed, so
-      // about 64 KB per CTA is in flight (one load at a time left HBM at 44 %)
+      // about 64 KB per CTA is in flight (one load at a time left HBM at 44 %;
+      // 1024 threads x 4 loads measured faster than 512 x 8)
       const float4* x4 = reinterpret_cast<const float4*>(xr);
       for (int base = threadIdx.x; base < n4; base += kBatch * kThreads) {
         float4 v[kBatch];
@@ -238,8 +239,8 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* lse, long long 
                                        (int)(kSmemCols * sizeof(float)));
   if (e != cudaSuccess) return e;
   // persistent: as many CTAs as fit (by shared memory) on every SM, rows strided
-  const int per_sm = staged ? (int)max((size_t)1, (size_t)(220 * 1024) / (smem + 1024)) : 4;
-  long long grid = (long long)n_sm * min(per_sm, 4);
+  const int per_sm = staged ? (int)max((size_t)1, (size_t)(220 * 1024) / (smem + 1024)) : 2;
+  long long grid = (long long)n_sm * min(per_sm, 2048 / kThreads);
   if (grid > rows) grid = rows;
   softmax_rows_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(x, y, lse, rows, cols, staged);
   return cudaGetLastError();

@@ -619,15 +619,19 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   using C = Bwd<D>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
   static_assert(C::TM_Y + 128 <= 512, "TMEM budget");
-  cudaError_t e = cudaFuncSetAttribute(fattn_bwd_kernel<D, VARLEN>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  static int prepared[64];
+  cudaError_t e = prepare_once(prepared, [] {
+    cudaError_t r = cudaFuncSetAttribute(fattn_bwd_kernel<D, VARLEN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (r != cudaSuccess) return r;
+    // the setmaxnreg split hands out exactly the launch's registers (128 per thread);
+    // with fewer at launch an increase would never be granted
+    cudaFuncAttributes fa;
+    r = cudaFuncGetAttributes(&fa, fattn_bwd_kernel<D, VARLEN>);
+    if (r != cudaSuccess) return r;
+    return fa.numRegs == 128 ? cudaSuccess : cudaErrorInvalidConfiguration;
+  });
   if (e != cudaSuccess) return e;
-  // the setmaxnreg split hands out exactly the launch's registers (128 per thread);
-  // with fewer at launch an increase would never be granted
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, fattn_bwd_kernel<D, VARLEN>);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs != 128) return cudaErrorInvalidConfiguration;
   const long long n_kb = (p.N + C::BK - 1) / C::BK;
   const long long blocks = n_kb * (VARLEN ? (long long)p.vl.B * p.vl.H : p.BH);
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

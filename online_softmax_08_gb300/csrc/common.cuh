@@ -88,6 +88,19 @@ __device__ __forceinline__ bool seq_view(const Varlen& vl, int dense_N, int seq,
   return true;
 }
 
+// Per-device one-time preparation of a kernel (its shared-memory opt-in and
+// register checks), so that later calls, including calls under stream capture
+// into a CUDA graph, make no attribute calls.  flags: one int per device.
+template <typename Prep>
+cudaError_t prepare_once(int (&flags)[64], Prep prep) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (__atomic_load_n(&flags[dev], __ATOMIC_ACQUIRE)) return cudaSuccess;
+  const cudaError_t e = prep();  // idempotent: two threads may both run it
+  if (e == cudaSuccess) __atomic_store_n(&flags[dev], 1, __ATOMIC_RELEASE);
+  return e;
+}
+
 // Launchers (one per translation unit).  Return cudaSuccess or the launch error.
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t stream);

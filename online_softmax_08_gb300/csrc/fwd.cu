@@ -512,15 +512,19 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   using C = Fwd<D>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
   static_assert(!(VARLEN && SPLIT), "split-KV is dense only");
-  cudaError_t e = cudaFuncSetAttribute(fattn_fwd_kernel<D, VARLEN, SPLIT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  static int prepared[64];
+  cudaError_t e = prepare_once(prepared, [] {
+    cudaError_t r = cudaFuncSetAttribute(fattn_fwd_kernel<D, VARLEN, SPLIT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (r != cudaSuccess) return r;
+    // the setmaxnreg split hands out at most the launch's registers; with fewer
+    // at launch an increase would never be granted
+    cudaFuncAttributes fa;
+    r = cudaFuncGetAttributes(&fa, fattn_fwd_kernel<D, VARLEN, SPLIT>);
+    if (r != cudaSuccess) return r;
+    return fa.numRegs >= C::REG_LAUNCH ? cudaSuccess : cudaErrorInvalidConfiguration;
+  });
   if (e != cudaSuccess) return e;
-  // the setmaxnreg split hands out at most the launch's registers; with fewer
-  // at launch an increase would never be granted
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, fattn_fwd_kernel<D, VARLEN, SPLIT>);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs < C::REG_LAUNCH) return cudaErrorInvalidConfiguration;
   const long long n_qb = ((SPLIT ? p.Nq : p.N) + 255) / 256;
   const long long blocks = n_qb * (VARLEN ? (long long)p.vl.B * p.vl.H : p.BH) *
                            (SPLIT ? p.n_splits : 1);

@@ -234,9 +234,11 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* lse, long long 
   if (rows <= 0 || cols <= 0) return cudaSuccess;
   const int staged = cols <= kSmemCols ? 1 : 0;
   const size_t smem = staged ? (size_t)((cols + 3) & ~3) * sizeof(float) : 0;
-  cudaError_t e = cudaFuncSetAttribute(softmax_rows_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)(kSmemCols * sizeof(float)));
+  static int prepared[64];
+  cudaError_t e = prepare_once(prepared, [] {
+    return cudaFuncSetAttribute(softmax_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(kSmemCols * sizeof(float)));
+  });
   if (e != cudaSuccess) return e;
   // persistent: as many CTAs as fit (by shared memory) on every SM, rows strided
   const int per_sm = staged ? (int)max((size_t)1, (size_t)(220 * 1024) / (smem + 1024)) : 2;

@@ -33,9 +33,10 @@ if ROOT not in sys.path:
 import torch  # noqa: E402
 
 from online_softmax_08_gb300.inputs import (DECODE_WORKLOADS, HEADLINE,  # noqa: E402
-                                            SOFTMAX_WORKLOADS, VARLEN_WORKLOADS, WORKLOADS,
-                                            default_scale, make_inputs, make_softmax_input,
-                                            make_varlen_inputs, varlen_lengths)
+                                            HOST_WORKLOADS, SOFTMAX_WORKLOADS, VARLEN_WORKLOADS,
+                                            WORKLOADS, default_scale, make_host_inputs,
+                                            make_inputs, make_softmax_input, make_varlen_inputs,
+                                            varlen_lengths)
 
 METRIC = "attention fwd/bwd TFLOP/s, N=8192 d=128 bf16 causal; % of GB300 BF16 peak"
 UNIT = "TFLOP/s"
@@ -603,6 +604,76 @@ def run_gpu_softmax(args):
     return 0
 
 
+# ------------------------------------------------------------------ host-CPU path
+
+def run_host(args):
+    """Profiling mode for the host-CPU flash-style forward (libfattn_host): fp32
+    on all host cores, against the fp32 multiply-add peak measured on the same
+    threads.  No GPU is used."""
+    import numpy as np
+
+    import oracle
+    from online_softmax_08_gb300 import fattn_host
+
+    w = HOST_WORKLOADS[args.workload]
+    B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"]
+    q, k, v = make_host_inputs(B, H, N, d, w["seed"])
+    scale = default_scale(d)
+    lib = fattn_host.load()
+    o = np.empty_like(q)
+    lse = np.empty((B, H, N), dtype=np.float32)
+    step = lambda: fattn_host.fattn_host_fwd(q, k, v, o, lse, B, H, N, d, scale, causal)
+    for _ in range(args.warmup):
+        step()
+    K = args.steps
+    t0 = time.perf_counter()
+    for _ in range(K):
+        step()
+    el = time.perf_counter() - t0
+    fwd_flops, _ = flops(B, H, N, d, causal)
+    ms = el / K * 1e3
+    value = fwd_flops / (el / K) / 1e12
+    # the public call, with output allocation and argument checks
+    t0 = time.perf_counter()
+    for _ in range(K):
+        fattn_host.forward(q, k, v, scale, causal)
+    e2e = fwd_flops * K / (time.perf_counter() - t0) / 1e12
+    threads = lib.fattn_host_max_threads()
+    peak = lib.fattn_host_fma_peak_gflops(0, 0.5) / 1e3
+    line = {
+        "metric": "attention fwd TFLOP/s on the host CPU cores, fp32",
+        "value": value, "unit": UNIT, "n_gpus": 0, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d, "causal": causal,
+                   "threads": threads, "device": "host cores (no GPU)"},
+        "roofline": {"kernel": "fattn_host_fwd", "bound": "alu", "achieved": value,
+                     "peak": peak, "unit": "TFLOP/s", "frac": value / peak,
+                     "peak_source": "measured: fp32 fused multiply-add loop on the same %d "
+                                    "threads" % threads, "traffic": None},
+        "cpu_baseline": None, "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": 0,
+                                      "d2h_bytes_per_step": 0},
+        "gpu_launches": 0, "clocks": None,
+    }
+    if not args.no_cpu_baseline:
+        # the fp64 oracle on head 0 of the same inputs, repeated for a few seconds
+        qh, kh, vh = (x[:1, :1].astype(np.float64) for x in (q, k, v))
+        done, n, t0 = 0.0, 0, time.perf_counter()
+        while True:
+            oracle.attention_fwd(qh, kh, vh, scale, causal)
+            done += flops(1, 1, N, d, causal)[0]
+            n += 1
+            t = time.perf_counter() - t0
+            if t >= 5.0:
+                break
+        line["cpu_baseline"] = {"value": done / t / 1e12, "unit": UNIT,
+                                "cores": oracle.max_threads(), "kind": "oracle",
+                                "sample": "fp64 oracle forward of head 0 (N=%d), %d times "
+                                          "(%.1f s)" % (N, n, t)}
+    print(json.dumps(_clean(line)), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -611,7 +682,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE,
                     choices=sorted(WORKLOADS) + sorted(VARLEN_WORKLOADS) + sorted(DECODE_WORKLOADS)
-                    + sorted(SOFTMAX_WORKLOADS),
+                    + sorted(SOFTMAX_WORKLOADS) + sorted(HOST_WORKLOADS),
                     help="profiling only: the benchmark's workload is the default")
     ap.add_argument("--pass", dest="passes", default="both", choices=["both", "fwd", "bwd"],
                     help="profiling only: time one pass; a benchmark step is both")
@@ -628,6 +699,8 @@ def main(argv=None):
         return run_gpu_decode(args)
     if args.workload in SOFTMAX_WORKLOADS:
         return run_gpu_softmax(args)
+    if args.workload in HOST_WORKLOADS:
+        return run_host(args)
     return run_gpu(args)
 
 

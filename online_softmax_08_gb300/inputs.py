@@ -125,3 +125,17 @@ def make_softmax_input(rows, cols, seed, scale=30.0):
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
     return torch.randn((rows, cols), generator=g, dtype=torch.float32) * float(scale)
+
+
+# Host-CPU workloads (the flash-style forward on the host cores): fp32 inputs
+# drawn like make_inputs (N(0, 1), order Q, K, V, rounded to bf16 and widened
+# back, so the values are the same kind the GPU path sees).  The shape is a
+# small-model attention layer at a long context: 16 heads of d = 64, 4096 tokens.
+HOST_WORKLOADS = {
+    "host_b1h16_n4096_d64_causal": dict(B=1, H=16, N=4096, d=64, seed=1244, causal=True),
+}
+
+
+def make_host_inputs(B, H, N, d, seed, q_std=1.0, v_dist="normal"):
+    """fp32 numpy arrays (q, k, v) of shape [B, H, N, d] (bf16-representable values)."""
+    return tuple(t.float().numpy() for t in make_inputs(B, H, N, d, seed, q_std, v_dist))

@@ -1,12 +1,13 @@
-"""The C-ABI library loads and exports every entry point include/fattn.h
-declares; argument checks that fail before any device work run on the CPU."""
+"""The C-ABI libraries load and export every entry point their headers declare
+(include/fattn.h: libfattn; include/fattn_host.h: libfattn_host); argument
+checks that fail before any device work run on the CPU."""
 import os
 import re
 
 import pytest
 
 from online_softmax_08_gb300 import build as fbuild
-from online_softmax_08_gb300 import fattn
+from online_softmax_08_gb300 import fattn, fattn_host
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -17,22 +18,33 @@ def lib():
     return fattn.load()
 
 
-def _declared():
-    names = set()
-    for fn in os.listdir(os.path.join(ROOT, "include")):
-        if fn.endswith(".h"):
-            src = open(os.path.join(ROOT, "include", fn)).read()
-            names |= set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(fattn_\w+)\s*\(", src,
-                                    flags=re.M))
-    return names
+def _declared(header):
+    src = open(os.path.join(ROOT, "include", header)).read()
+    return set(re.findall(r"^\s*(?:int|size_t|double|void|const char\*)\s+(fattn_\w+)\s*\(",
+                          src, flags=re.M))
+
+
+def test_headers_are_the_two_libraries():
+    assert sorted(f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")) == \
+        ["fattn.h", "fattn_host.h"]
 
 
 def test_every_declared_symbol_is_exported_and_bound(lib):
-    declared = _declared()
+    declared = _declared("fattn.h")
     assert {"fattn_fwd", "fattn_bwd", "fattn_bwd_workspace_bytes"} <= declared
     for name in declared:
         assert hasattr(lib, name), name
         assert name in fattn.SIGNATURES, name
+    assert set(fattn.SIGNATURES) == declared
+
+
+def test_every_host_symbol_is_exported_and_bound(lib):
+    host = fattn_host.load()
+    declared = _declared("fattn_host.h")
+    assert {"fattn_host_fwd", "fattn_host_fma_peak_gflops"} <= declared
+    for name in declared:
+        assert hasattr(host, name), name
+    assert set(fattn_host.SIGNATURES) == declared
 
 
 def test_status_strings(lib):

@@ -345,8 +345,10 @@ def run_gpu(args):
                 else None,
                 "algorithmic_bytes": fwd_bytes}
 
-    # end to end through the C-ABI with host buffers: pinned H2D of Q, K, V, dO,
-    # forward, backward, D2H of O, LSE, dQ, dK, dV
+    # end to end through the C-ABI with host buffers: fattn_fwd_bwd_host copies
+    # Q, K, V, dO in from pinned host memory, runs the forward and the backward
+    # and copies O, LSE, dQ, dK, dV back, chunk by chunk of heads with the copies
+    # and the kernels overlapped
     e2e = None
     if not args.no_e2e and args.passes == "both":
         pin = [x.pin_memory() for x in host]
@@ -357,13 +359,13 @@ def run_gpu(args):
                   torch.empty_like(dv, device="cpu").pin_memory()]
         h2d = sum(x.numel() * x.element_size() for x in pin)
         d2h = sum(x.numel() * x.element_size() for x in outs_h)
+        hpc = int(args.e2e_chunk)
+        e2e_ws_bytes = fattn.fattn_fwd_bwd_host_workspace_bytes(B, H, N, d, hpc)
+        e2e_ws = torch.empty(e2e_ws_bytes, dtype=torch.uint8, device=device)
 
         def e2e_step():
-            for dst, src in zip((q, k, v, do), pin):
-                dst.copy_(src, non_blocking=True)
-            step()
-            for dst, src in zip(outs_h, (o, lse, dq, dk, dv)):
-                dst.copy_(src, non_blocking=True)
+            fattn.fattn_fwd_bwd_host(*pin, *outs_h, B, H, N, d, scale, causal, hpc, e2e_ws,
+                                     e2e_ws_bytes, stream)
 
         for _ in range(2):
             e2e_step()
@@ -376,9 +378,13 @@ def run_gpu(args):
         b.record(stream)
         torch.cuda.synchronize(device)
         barrier(world)
+        assert fattn.fattn_device_error() == 0, "an in-kernel wait timed out"
         e2e_ms = max_over_ranks(a.elapsed_time(b), world, device) / K
         e2e = {"value": job_tflops(world, step_flops, e2e_ms), "unit": UNIT,
-               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "api": "fattn_fwd_bwd_host (pinned host buffers)",
+               "heads_per_chunk": hpc if hpc > 0 else "library's choice"}
+        del e2e_ws
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == HEADLINE:
@@ -688,6 +694,8 @@ def main(argv=None):
                     help="profiling only: time one pass; a benchmark step is both")
     ap.add_argument("--splits", default=0, help="decode workloads: key ranges (0 = automatic)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-chunk", default=0,
+                    help="heads per chunk of the end-to-end leg (0 = the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps

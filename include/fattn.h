@@ -200,6 +200,35 @@ int fattn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o
                       const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
                       int H, int N, int d, float scale, int causal, void* stream);
 
+/* Bytes of DEVICE workspace fattn_fwd_bwd_host needs: three staging slots,
+ * each holding Q, K, V, dO, O, dQ, dK, dV and LSE of one chunk of heads plus
+ * that chunk's backward workspace.  heads_per_chunk = 0 selects the library's
+ * chunk size for the current device (the same one fattn_fwd_bwd_host picks
+ * for 0).  Returns 0 for invalid sizes. */
+size_t fattn_fwd_bwd_host_workspace_bytes(int B, int H, int N, int d, int heads_per_chunk);
+
+/* Forward and backward of tensors in HOST memory: the same results as
+ * fattn_fwd followed by fattn_bwd.  q, k, v, dout are HOST pointers to bf16
+ * [B,H,N,d]; o, dq, dk, dv HOST pointers to bf16 [B,H,N,d] and lse to fp32
+ * [B,H,N], all written by the call.  Every (b, h) slice is an independent
+ * problem ("FlashAttention tiles exact softmax without materializing the score
+ * matrix", opening equations), so the slices move through `workspace` (DEVICE,
+ * 256-byte aligned, fattn_fwd_bwd_host_workspace_bytes large) in chunks of
+ * heads_per_chunk consecutive slices (0 = the library's choice; the first
+ * chunk is half as large so that the kernels start sooner), and the copy in of
+ * one chunk, the kernels of the previous one and the copy out of the one
+ * before run at the same time on three streams the library keeps per device.  Asynchronous on `stream` like the other entry points: the host
+ * buffers must stay untouched until `stream` has reached this call's end.
+ * The copies overlap only when the host buffers are page-locked
+ * (cudaHostAlloc or cudaHostRegister); pageable memory gives the same results
+ * with the copies serialised.  Calls from several host threads are
+ * serialised while they enqueue.  Errors: those of fattn_fwd and fattn_bwd;
+ * FATTN_ERR_WORKSPACE for a missing, misaligned or short workspace. */
+int fattn_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dout, void* o,
+                       float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                       float scale, int causal, int heads_per_chunk, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
 /* Tile shape used by a pass (0 = forward, 1 = backward) for head size d:
  * rows of Q per tile and keys per K/V tile.  Returns FATTN_OK or
  * FATTN_ERR_UNSUPPORTED. */

@@ -51,8 +51,7 @@ namespace {
 
 constexpr int BQ = 64;   // query rows per task
 constexpr int BK = 64;   // keys per block
-constexpr int CJ = 16;   // floats per vector (one AVX-512 register, four NEON registers)
-constexpr int RB = 4;    // query rows per register block
+constexpr int CJ = 16;   // columns per chunk: the unit of every vector loop and reduction
 constexpr int DMAX = FATTN_HOST_MAX_D;
 
 constexpr double kLn2 = 0.693147180559945309417232121458176568;
@@ -70,31 +69,41 @@ constexpr float kC0 = (float)taylor(0), kC1 = (float)taylor(1), kC2 = (float)tay
 // adding 1.5 * 2^23 rounds a float of magnitude below 2^22 to an integer
 constexpr float kRound = 12582912.f;
 
-// GCC vector extensions: the compiler maps them onto whatever vector unit the
-// target has (AVX-512, AVX2, SSE, NEON); no intrinsics
-typedef float vf __attribute__((vector_size(CJ * sizeof(float))));
-typedef int vi __attribute__((vector_size(CJ * sizeof(int))));
-typedef float vf_u __attribute__((vector_size(CJ * sizeof(float)), aligned(4)));
-
-#if defined(__x86_64__) && defined(__GNUC__) && !defined(__clang__)
-// the hot functions are also compiled for x86-64-v3 (AVX2 + FMA) and
-// x86-64-v4 (AVX-512); the loader picks the best the host supports
-#define HOST_CLONES __attribute__((target_clones("arch=x86-64-v4", "arch=x86-64-v3", "default")))
-#else
-#define HOST_CLONES
-#endif
 #define HOST_INLINE static inline __attribute__((always_inline))
 
-HOST_INLINE vf load(const float* p) { return *(const vf_u*)p; }
-HOST_INLINE void store(float* p, vf x) { *(vf_u*)p = x; }
-HOST_INLINE vf splat(float x) { return vf{} + x; }
+// GCC vector extensions of W floats, W the width of the target's vector
+// registers (4 for NEON and SSE, 8 for AVX2, 16 for AVX-512), so that every
+// vector lives in a register; no intrinsics.  A chunk of CJ columns is CJ / W
+// vectors.
+template <int W>
+struct Vec {
+  typedef float f __attribute__((vector_size(W * sizeof(float))));
+  typedef int i __attribute__((vector_size(W * sizeof(int))));
+  typedef float fu __attribute__((vector_size(W * sizeof(float)), aligned(4)));
+};
+
+template <int W>
+HOST_INLINE typename Vec<W>::f vload(const float* p) {
+  return *(const typename Vec<W>::fu*)p;
+}
+template <int W>
+HOST_INLINE void vstore(float* p, typename Vec<W>::f x) {
+  *(typename Vec<W>::fu*)p = x;
+}
+template <int W>
+HOST_INLINE typename Vec<W>::f vsplat(float x) {
+  return typename Vec<W>::f{} + x;
+}
 
 // 2^t for t <= 0, lane by lane
-HOST_INLINE vf exp2_nonpos(vf t) {
-  t = t < -127.f ? splat(-127.f) : t;  // also maps -inf; 2^-127 and below become 0 below
-  const vf n = (t + kRound) - kRound;  // nearest integer
-  const vf f = t - n;                  // exact, in [-1/2, 1/2]
-  vf p = splat(kC7);
+template <int W>
+HOST_INLINE typename Vec<W>::f exp2_nonpos(typename Vec<W>::f t) {
+  typedef typename Vec<W>::f vf;
+  typedef typename Vec<W>::i vi;
+  t = t < -127.f ? vsplat<W>(-127.f) : t;  // also maps -inf; 2^-127 and below become 0 below
+  const vf n = (t + kRound) - kRound;      // nearest integer
+  const vf f = t - n;                      // exact, in [-1/2, 1/2]
+  vf p = vsplat<W>(kC7);
   p = p * f + kC6;
   p = p * f + kC5;
   p = p * f + kC4;
@@ -104,6 +113,19 @@ HOST_INLINE vf exp2_nonpos(vf t) {
   p = p * f + kC0;
   const vi e = __builtin_convertvector(n, vi) + 127;  // 0 for n = -127: the scale is then +0
   return p * (vf)(e << 23);
+}
+
+// Reductions of a chunk's CJ logical lanes (lane u = x[u / W][u % W]) by one
+// fixed tree: for w = CJ/2, ..., 1, lane u takes op(lane u, lane u + w).  The
+// steps with w >= W combine whole vectors, the rest run inside x[0]; the tree,
+// and so the result, is the same for every W.
+template <int W, class Op>
+HOST_INLINE float chunk_reduce(typename Vec<W>::f (&x)[CJ / W], Op op) {
+  for (int w = CJ / 2; w >= W; w >>= 1)
+    for (int t = 0; t < w / W; ++t) x[t] = op(x[t], x[t + w / W]);
+  for (int w = W / 2; w > 0; w >>= 1)
+    for (int u = 0; u < w; ++u) x[0][u] = op(x[0][u], x[0][u + w]);
+  return x[0][0];
 }
 
 struct Problem {
@@ -116,7 +138,7 @@ struct Problem {
   float *kt, *vp;  // packed blocks: [BH][nkb][Dp][BK] and [BH][nkb][BK][Dp]
 };
 
-HOST_CLONES void pack_block(const Problem& pr, long long bh, int kb) {
+void pack_block(const Problem& pr, long long bh, int kb) {
   const int j0 = kb * BK, kn = std::min(BK, pr.N - j0), d = pr.d, Dp = pr.Dp;
   const size_t blk = ((size_t)bh * pr.nkb + kb) * (size_t)Dp * BK;
   float* __restrict kt = pr.kt + blk;
@@ -144,90 +166,99 @@ struct Scratch {
   float m[BQ], l[BQ], alpha[BQ];
 };
 
-// s[r][:] = q[r] . kt, for RB rows at a time
+// s[r][:] = q[r] . kt, for RB rows and one chunk of keys at a time
+template <int W, int RB>
 HOST_INLINE void block_scores(const float* __restrict q, const float* __restrict kt,
                               float* __restrict s, int Dp, int rows) {
+  typedef typename Vec<W>::f vf;
+  constexpr int NV = CJ / W;
   for (int r0 = 0; r0 < rows; r0 += RB) {
     const float* q0 = q + (size_t)r0 * Dp;
     for (int j0 = 0; j0 < BK; j0 += CJ) {
-      vf acc[RB];
-#pragma GCC unroll 4
-      for (int rr = 0; rr < RB; ++rr) acc[rr] = vf{};
+      vf acc[RB][NV];
+      for (int rr = 0; rr < RB; ++rr)
+        for (int t = 0; t < NV; ++t) acc[rr][t] = vf{};
       const float* kc = kt + j0;
       for (int c = 0; c < Dp; ++c, kc += BK) {
-        const vf kv = load(kc);
-#pragma GCC unroll 4
-        for (int rr = 0; rr < RB; ++rr) acc[rr] = q0[(size_t)rr * Dp + c] * kv + acc[rr];
+        vf kv[NV];
+        for (int t = 0; t < NV; ++t) kv[t] = vload<W>(kc + t * W);
+        for (int rr = 0; rr < RB; ++rr) {
+          const float a = q0[(size_t)rr * Dp + c];
+          for (int t = 0; t < NV; ++t) acc[rr][t] = a * kv[t] + acc[rr][t];
+        }
       }
-#pragma GCC unroll 4
-      for (int rr = 0; rr < RB; ++rr) store(s + (size_t)(r0 + rr) * BK + j0, acc[rr]);
+      for (int rr = 0; rr < RB; ++rr)
+        for (int t = 0; t < NV; ++t) vstore<W>(s + (size_t)(r0 + rr) * BK + j0 + t * W, acc[rr][t]);
     }
   }
 }
 
-// o[r] = alpha[r] o[r] + sum_jj p[r][jj] vp[jj], for RB rows at a time
+// o[r] = alpha[r] o[r] + sum_jj p[r][jj] vp[jj], for RB rows and one chunk of columns at a time
+template <int W, int RB>
 HOST_INLINE void block_accumulate(const float* __restrict p, const float* __restrict vp,
                                   float* __restrict o, const float* __restrict alpha, int Dp,
                                   int rows) {
+  typedef typename Vec<W>::f vf;
+  constexpr int NV = CJ / W;
   for (int r0 = 0; r0 < rows; r0 += RB) {
     const float* p0 = p + (size_t)r0 * BK;
     for (int c0 = 0; c0 < Dp; c0 += CJ) {
-      vf acc[RB];
-#pragma GCC unroll 4
-      for (int rr = 0; rr < RB; ++rr)
-        acc[rr] = load(o + (size_t)(r0 + rr) * Dp + c0) * alpha[r0 + rr];
+      vf acc[RB][NV];
+      for (int rr = 0; rr < RB; ++rr) {
+        const float a = alpha[r0 + rr];
+        for (int t = 0; t < NV; ++t) acc[rr][t] = vload<W>(o + (size_t)(r0 + rr) * Dp + c0 + t * W) * a;
+      }
       const float* vr = vp + c0;
       for (int jj = 0; jj < BK; ++jj, vr += Dp) {
-        const vf vv = load(vr);
-#pragma GCC unroll 4
-        for (int rr = 0; rr < RB; ++rr) acc[rr] = p0[(size_t)rr * BK + jj] * vv + acc[rr];
+        vf vv[NV];
+        for (int t = 0; t < NV; ++t) vv[t] = vload<W>(vr + t * W);
+        for (int rr = 0; rr < RB; ++rr) {
+          const float pv = p0[(size_t)rr * BK + jj];
+          for (int t = 0; t < NV; ++t) acc[rr][t] = pv * vv[t] + acc[rr][t];
+        }
       }
-#pragma GCC unroll 4
-      for (int rr = 0; rr < RB; ++rr) store(o + (size_t)(r0 + rr) * Dp + c0, acc[rr]);
+      for (int rr = 0; rr < RB; ++rr)
+        for (int t = 0; t < NV; ++t) vstore<W>(o + (size_t)(r0 + rr) * Dp + c0 + t * W, acc[rr][t]);
     }
   }
 }
 
-// lanes of x combined pairwise in a fixed order: (0..7 with 8..15), then halves again
-HOST_INLINE float lane_max(vf x) {
-  for (int w = CJ / 2; w > 0; w >>= 1)
-    for (int u = 0; u < w; ++u) x[u] = x[u + w] > x[u] ? x[u + w] : x[u];
-  return x[0];
-}
-HOST_INLINE float lane_sum(vf x) {
-  for (int w = CJ / 2; w > 0; w >>= 1)
-    for (int u = 0; u < w; ++u) x[u] = x[u] + x[u + w];
-  return x[0];
-}
-
 // the online update of (m, l) for one row of scores; the row becomes P
+template <int W>
 HOST_INLINE void row_update(float* __restrict sr, float& m, float& l, float& alpha) {
-  vf mx = load(sr);
-#pragma GCC unroll 4
-  for (int j = CJ; j < BK; j += CJ) {
-    const vf x = load(sr + j);
-    mx = x > mx ? x : mx;
-  }
-  const float mb = lane_max(mx);
+  typedef typename Vec<W>::f vf;
+  constexpr int NV = CJ / W;
+  auto vmax = [](auto a, auto b) { return b > a ? b : a; };
+  auto vadd = [](auto a, auto b) { return a + b; };
+  vf mx[NV];
+  for (int t = 0; t < NV; ++t) mx[t] = vload<W>(sr + t * W);
+  for (int j = CJ; j < BK; j += CJ)
+    for (int t = 0; t < NV; ++t) {
+      const vf x = vload<W>(sr + j + t * W);
+      mx[t] = x > mx[t] ? x : mx[t];
+    }
+  const float mb = chunk_reduce<W>(mx, vmax);
   const float m_new = mb > m ? mb : m;
   if (m_new == -INFINITY) {  // nothing visible in this row yet
     alpha = 1.f;
-    for (int j = 0; j < BK; j += CJ) store(sr + j, vf{});
+    for (int j = 0; j < BK; ++j) sr[j] = 0.f;
     return;
   }
-  alpha = exp2_nonpos(splat(m - m_new))[0];  // 0 on the first visible block (m = -inf)
-  vf ls = vf{};
-#pragma GCC unroll 4
-  for (int j = 0; j < BK; j += CJ) {
-    const vf pj = exp2_nonpos(load(sr + j) - m_new);
-    store(sr + j, pj);
-    ls += pj;
-  }
-  l = alpha * l + lane_sum(ls);
+  alpha = exp2_nonpos<W>(vsplat<W>(m - m_new))[0];  // 0 on the first visible block (m = -inf)
+  vf ls[NV];
+  for (int t = 0; t < NV; ++t) ls[t] = vf{};
+  for (int j = 0; j < BK; j += CJ)
+    for (int t = 0; t < NV; ++t) {
+      const vf pj = exp2_nonpos<W>(vload<W>(sr + j + t * W) - m_new);
+      vstore<W>(sr + j + t * W, pj);
+      ls[t] += pj;
+    }
+  l = alpha * l + chunk_reduce<W>(ls, vadd);
   m = m_new;
 }
 
-HOST_CLONES void run_task(const Problem& pr, Scratch& sc, long long bh, int qt) {
+template <int W, int RB>
+HOST_INLINE void run_task_w(const Problem& pr, Scratch& sc, long long bh, int qt) {
   const int d = pr.d, Dp = pr.Dp, N = pr.N;
   const int i0 = qt * BQ, rows = std::min(BQ, N - i0);
   const int rows_p = (rows + RB - 1) / RB * RB;
@@ -247,7 +278,7 @@ HOST_CLONES void run_task(const Problem& pr, Scratch& sc, long long bh, int qt) 
   for (int kb = 0; kb < kb_end; ++kb) {
     const int j0 = kb * BK;
     const size_t blk = ((size_t)bh * pr.nkb + kb) * (size_t)Dp * BK;
-    block_scores(sc.q, pr.kt + blk, sc.s, Dp, rows_p);
+    block_scores<W, RB>(sc.q, pr.kt + blk, sc.s, Dp, rows_p);
     // masks before the block max: keys past N, and (causal) keys after the query
     const bool ragged = j0 + BK > N;
     const bool diag = pr.causal && j0 + BK - 1 > i0;
@@ -260,13 +291,13 @@ HOST_CLONES void run_task(const Problem& pr, Scratch& sc, long long bh, int qt) 
     }
     for (int r = 0; r < rows_p; ++r) {
       if (r < rows) {
-        row_update(sc.s + (size_t)r * BK, sc.m[r], sc.l[r], sc.alpha[r]);
+        row_update<W>(sc.s + (size_t)r * BK, sc.m[r], sc.l[r], sc.alpha[r]);
       } else {  // padding rows stay zero
         sc.alpha[r] = 1.f;
         for (int jj = 0; jj < BK; ++jj) sc.s[(size_t)r * BK + jj] = 0.f;
       }
     }
-    block_accumulate(sc.s, pr.vp + blk, sc.o, sc.alpha, Dp, rows_p);
+    block_accumulate<W, RB>(sc.s, pr.vp + blk, sc.o, sc.alpha, Dp, rows_p);
   }
   // O = o~ / l;  LSE = m + ln l, back from base-2 units
   float* og = pr.o + ((size_t)bh * N + i0) * d;
@@ -277,6 +308,79 @@ HOST_CLONES void run_task(const Problem& pr, Scratch& sc, long long bh, int qt) 
     pr.lse[(size_t)bh * N + i0 + r] = (float)(((double)sc.m[r] + log2((double)l)) * kLn2);
   }
 }
+
+// multiply-add throughput: KV independent vector chains (enough to cover the
+// latency of every FMA pipe) on W-float vectors
+template <int W, int KV>
+HOST_INLINE float fma_loop_w(long long iters, float a, float b) {
+  typedef typename Vec<W>::f vf;
+  vf acc[KV];
+  for (int u = 0; u < KV; ++u) acc[u] = vsplat<W>((float)u * 1e-3f);
+  const vf va = vsplat<W>(a), vb = vsplat<W>(b);
+  for (long long it = 0; it < iters; ++it)
+#pragma GCC unroll 16
+    for (int u = 0; u < KV; ++u) acc[u] = acc[u] * va + vb;
+  // whole-vector adds, then the lanes of one vector (indexing the array by a
+  // run-time lane would keep it in memory through the loop above)
+  vf t = acc[0];
+#pragma GCC unroll 16
+  for (int u = 1; u < KV; ++u) t += acc[u];
+  float s = 0.f;
+#pragma GCC unroll 16
+  for (int i = 0; i < W; ++i) s += t[i];
+  return s;
+}
+
+template <int W>
+HOST_INLINE void exp2_array_w(const float* __restrict t, float* __restrict y, long long n) {
+  long long i = 0;
+  for (; i + W <= n; i += W) vstore<W>(y + i, exp2_nonpos<W>(vload<W>(t + i)));
+  if (i < n) {
+    float buf[W];
+    for (int u = 0; u < W; ++u) buf[u] = i + u < n ? t[i + u] : 0.f;
+    const typename Vec<W>::f r = exp2_nonpos<W>(vload<W>(buf));
+    for (long long u = 0; i + u < n; ++u) y[i + u] = r[u];
+  }
+}
+
+// One instance per vector unit.  Each is compiled for its own target, with the
+// templates above inlined into it, and picked at run time.
+struct Kernels {
+  void (*run_task)(const Problem&, Scratch&, long long, int);
+  float (*fma_loop)(long long, float, float);
+  void (*exp2_array)(const float*, float*, long long);
+  int flops_per_iter;  // 2 * KV * W
+};
+
+#define DEFINE_KERNELS(NAME, TARGET, W, RB, KV)                                          \
+  TARGET void NAME##_run(const Problem& pr, Scratch& sc, long long bh, int qt) {         \
+    run_task_w<W, RB>(pr, sc, bh, qt);                                                   \
+  }                                                                                      \
+  TARGET float NAME##_fma(long long it, float a, float b) {                              \
+    return fma_loop_w<W, KV>(it, a, b);                                                  \
+  }                                                                                      \
+  TARGET void NAME##_exp2(const float* t, float* y, long long n) { exp2_array_w<W>(t, y, n); } \
+  const Kernels NAME = {NAME##_run, NAME##_fma, NAME##_exp2, 2 * KV * W};
+
+#if defined(__x86_64__) && defined(__GNUC__) && !defined(__clang__)
+// AVX-512 (32 registers of 16 floats), AVX2 + FMA (16 of 8), SSE (16 of 4)
+DEFINE_KERNELS(k_avx512, __attribute__((target("arch=x86-64-v4"))), 16, 8, 8)
+DEFINE_KERNELS(k_avx2, __attribute__((target("arch=x86-64-v3"))), 8, 4, 8)
+DEFINE_KERNELS(k_sse, , 4, 2, 8)
+const Kernels& kernels() {
+  static const Kernels* k = [] {
+    __builtin_cpu_init();
+    if (__builtin_cpu_supports("x86-64-v4")) return &k_avx512;
+    if (__builtin_cpu_supports("x86-64-v3")) return &k_avx2;
+    return &k_sse;
+  }();
+  return *k;
+}
+#else
+// AArch64 NEON: 32 registers of 4 floats, four FMA pipes of four-cycle latency
+DEFINE_KERNELS(k_neon, , 4, 4, 16)
+const Kernels& kernels() { return k_neon; }
+#endif
 
 int threads_for(int n_threads) {
 #ifdef _OPENMP
@@ -290,33 +394,6 @@ int threads_for(int n_threads) {
 void* alloc_floats(size_t n) {
   const size_t bytes = (n * sizeof(float) + 63) / 64 * 64;
   return aligned_alloc(64, bytes ? bytes : 64);
-}
-
-// multiply-add throughput: KV independent vector chains, enough to cover the
-// latency of every FMA pipe
-constexpr int KV = 8;
-
-HOST_CLONES float fma_loop(long long iters, float a, float b) {
-  vf acc[KV];
-  for (int u = 0; u < KV; ++u) acc[u] = splat((float)u * 1e-3f);
-  const vf va = splat(a), vb = splat(b);
-  for (long long it = 0; it < iters; ++it)
-#pragma GCC unroll 8
-    for (int u = 0; u < KV; ++u) acc[u] = acc[u] * va + vb;
-  vf s = vf{};
-  for (int u = 0; u < KV; ++u) s += acc[u];
-  return lane_sum(s);
-}
-
-HOST_CLONES void exp2_array(const float* __restrict t, float* __restrict y, long long n) {
-  long long i = 0;
-  for (; i + CJ <= n; i += CJ) store(y + i, exp2_nonpos(load(t + i)));
-  if (i < n) {
-    float buf[CJ];
-    for (int u = 0; u < CJ; ++u) buf[u] = i + u < n ? t[i + u] : 0.f;
-    const vf r = exp2_nonpos(load(buf));
-    for (long long u = 0; i + u < n; ++u) y[i + u] = r[u];
-  }
 }
 
 }  // namespace
@@ -348,6 +425,7 @@ int fattn_host_fwd(const float* q, const float* k, const float* v, float* o, flo
     free(pr.vp);
     return FATTN_HOST_ERR_NO_MEMORY;
   }
+  const Kernels& kern = kernels();
   const long long n_blocks = BH * pr.nkb;
   const long long n_tasks = BH * pr.nqt;
   const int nt = (int)std::max(1LL, std::min<long long>(threads_for(n_threads), n_tasks));
@@ -375,7 +453,7 @@ int fattn_host_fwd(const float* q, const float* k, const float* v, float* o, flo
     for (long long t = 0; t < n_tasks; ++t) {
       if (!ok) continue;
       const int qt = pr.causal ? pr.nqt - 1 - (int)(t / BH) : (int)(t / BH);
-      run_task(pr, sc, t % BH, qt);
+      kern.run_task(pr, sc, t % BH, qt);
     }
     free(sc.q);
     free(sc.o);
@@ -390,6 +468,7 @@ int fattn_host_max_threads(void) { return threads_for(0); }
 
 double fattn_host_fma_peak_gflops(int n_threads, double seconds) {
   const int nt = threads_for(n_threads);
+  const Kernels& kern = kernels();
   if (!(seconds > 0.0)) seconds = 0.2;
   // calibrate the iteration count on one thread
   long long iters = 1 << 16;
@@ -397,7 +476,7 @@ double fattn_host_fma_peak_gflops(int n_threads, double seconds) {
   volatile float sink = 0.f;
   for (;;) {
     const auto t0 = std::chrono::steady_clock::now();
-    sink = sink + fma_loop(iters, 0.999999f, 1e-6f);
+    sink = sink + kern.fma_loop(iters, 0.999999f, 1e-6f);
     el = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
     if (el >= seconds * 0.25 || iters >= (1LL << 40)) break;
     iters *= 2;
@@ -409,14 +488,14 @@ double fattn_host_fma_peak_gflops(int n_threads, double seconds) {
 #ifdef _OPENMP
 #pragma omp parallel num_threads(nt) reduction(+ : total)
 #endif
-  total += fma_loop(iters, 0.999999f, 1e-6f);
+  total += kern.fma_loop(iters, 0.999999f, 1e-6f);
   el = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
   sink = sink + total;
-  return 2.0 * KV * CJ * (double)iters * nt / el / 1e9;
+  return (double)kern.flops_per_iter * (double)iters * nt / el / 1e9;
 }
 
 void fattn_host_exp2(const float* t, float* y, long long n) {
-  if (t && y && n > 0) exp2_array(t, y, n);
+  if (t && y && n > 0) kernels().exp2_array(t, y, n);
 }
 
 }  // extern "C"

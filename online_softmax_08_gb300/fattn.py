@@ -45,6 +45,9 @@ SIGNATURES = {
     "fattn_fwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "fattn_bwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
                               _i, _f, _i, _vp, _sz, _vp]),
+    "fattn_fwd_bwd_host_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "fattn_fwd_bwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f,
+                                _i, _i, _vp, _sz, _vp]),
     "fattn_status_string": (ctypes.c_char_p, [_i]),
 }
 
@@ -161,6 +164,20 @@ def fattn_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, cu_seqlens, B, H, max_seql
         _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 
+def fattn_fwd_bwd_host_workspace_bytes(B, H, N, d, heads_per_chunk=0):
+    return int(load().fattn_fwd_bwd_host_workspace_bytes(B, H, N, d, int(heads_per_chunk)))
+
+
+def fattn_fwd_bwd_host(q, k, v, do, o, lse, dq, dk, dv, B, H, N, d, scale, causal,
+                       heads_per_chunk, workspace, workspace_bytes, stream=None):
+    """q, k, v, do, o, lse, dq, dk, dv: HOST tensors (pinned for overlap) or addresses;
+    workspace: a device tensor or address."""
+    _check("fattn_fwd_bwd_host", load().fattn_fwd_bwd_host(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(o), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H,
+        N, d, float(scale), int(bool(causal)), int(heads_per_chunk), _ptr(workspace),
+        int(workspace_bytes), _stream(stream)))
+
+
 def fattn_tile_sizes(d, pass_):
     bq, bk = ctypes.c_int(0), ctypes.c_int(0)
     _check("fattn_tile_sizes", load().fattn_tile_sizes(d, pass_, ctypes.byref(bq), ctypes.byref(bk)))
@@ -216,6 +233,32 @@ def backward(q, k, v, o, lse, do, scale, causal, workspace=None, stream=None):
     fattn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, workspace,
               workspace.numel() * workspace.element_size(), stream)
     return dq, dk, dv
+
+
+def forward_backward_host(q, k, v, do, scale, causal, heads_per_chunk=0, workspace=None,
+                          device=None, stream=None):
+    """Forward and backward of HOST bf16 tensors [B,H,N,d] through the device:
+    returns HOST (o, lse, dq, dk, dv), page-locked.  The call is asynchronous on
+    the stream; synchronise before reading the results."""
+    B, H, N, d = _shape(q)
+    device = torch.device("cuda") if device is None else torch.device(device)
+    with torch.cuda.device(device):
+        if stream is None:
+            stream = torch.cuda.current_stream(device)
+        nbytes = fattn_fwd_bwd_host_workspace_bytes(B, H, N, d, heads_per_chunk)
+        own = workspace is None
+        if own:
+            workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+        o, dq, dk, dv = (torch.empty(q.shape, dtype=torch.bfloat16).pin_memory() for _ in range(4))
+        lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        fattn_fwd_bwd_host(q, k, v, do, o, lse, dq, dk, dv, B, H, N, d, scale, causal,
+                           heads_per_chunk, workspace, workspace.numel() * workspace.element_size(),
+                           stream)
+        if own and isinstance(stream, torch.cuda.Stream):
+            # the workspace is in use until `stream` passes the call: keep the
+            # allocator from handing it out before then
+            workspace.record_stream(stream)
+    return o, lse, dq, dk, dv
 
 
 def forward_varlen(q, k, v, cu_seqlens, max_seqlen, scale, causal, stream=None):

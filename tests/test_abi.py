@@ -82,3 +82,28 @@ def test_argument_checks_before_any_device_call(lib):
     assert lib.fattn_bwd(a, a, a, a, a, a, a, a, a, 1, 1, 128, 128, 0.1, 1, a + 16, 1 << 30,
                          None) == 4
     assert lib.fattn_bwd(a, a, a, a, a, a, a, a, a, 1, 1, 128, 128, 0.1, 1, a, 16, None) == 4
+
+
+def test_host_staged_argument_checks_before_any_device_call(lib):
+    a = 1 << 20
+    ws = 1 << 24  # 256-byte aligned, never dereferenced
+    args = lambda **kw: [kw.get(n, a) for n in ("q", "k", "v", "do", "o", "lse", "dq", "dk", "dv")]
+    call = lambda ptrs, B=1, H=4, N=256, d=64, scale=0.1, hpc=2, w=ws, wb=1 << 40: \
+        lib.fattn_fwd_bwd_host(*ptrs, B, H, N, d, scale, 1, hpc, w, wb, None)
+    assert call(args(q=None)) == 1
+    assert call(args(lse=None)) == 1
+    assert call(args(), d=80) == 2
+    assert call(args(), B=0) == 1
+    assert call(args(), scale=float("inf")) == 1
+    assert call(args(), hpc=-1) == 1
+    assert call(args(), w=None) == 4
+    assert call(args(), w=ws + 128) == 4
+    need = fattn.fattn_fwd_bwd_host_workspace_bytes(1, 4, 256, 64, 2)
+    assert call(args(), wb=need - 1) == 4
+    # three slots, each with 8 bf16 tiles, LSE and the backward's workspace of 2 heads
+    rows = 2 * 256
+    assert need == 3 * (8 * rows * 64 * 2 + rows * 4 + fattn.fattn_bwd_workspace_bytes(1, 2, 256, 64))
+    assert fattn.fattn_fwd_bwd_host_workspace_bytes(1, 4, 256, 96, 2) == 0
+    # a chunk larger than B*H is clipped to B*H
+    assert fattn.fattn_fwd_bwd_host_workspace_bytes(1, 4, 256, 64, 9) == \
+        fattn.fattn_fwd_bwd_host_workspace_bytes(1, 4, 256, 64, 4)

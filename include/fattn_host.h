@@ -22,7 +22,7 @@
  * Numerics.  fp32 throughout, multiply-adds fused where the host has a fused
  * multiply-add (every AArch64 host; x86-64 with AVX2/FMA), the exponential
  * evaluated by the library's own exp2 (a degree-7 Taylor polynomial of 2^f
- * after range reduction; within 1 ulp of 2^t on [-126, 0], 0 below -126.5).
+ * after range reduction; within 1.5 ulp of 2^t on [-126, 0], 0 below -126.5).
  * Every reduction runs in a fixed order: the result is the same, bit for bit,
  * for any thread count.  Inputs must be finite.
  *

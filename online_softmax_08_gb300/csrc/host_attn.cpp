@@ -166,11 +166,15 @@ struct Scratch {
   float m[BQ], l[BQ], alpha[BQ];
 };
 
-// s[r][:] = q[r] . kt, for RB rows and one chunk of keys at a time
-template <int W, int RB>
+// s[r][:] = q[r] . kt, for RB rows and one chunk of keys at a time.  LANES:
+// take four consecutive q values of a row as one vector and multiply by its
+// lanes (one load per four multiply-adds per row; AArch64 has a multiply-add
+// by vector lane); otherwise broadcast each q value from memory (x86).
+template <int W, int RB, bool LANES>
 HOST_INLINE void block_scores(const float* __restrict q, const float* __restrict kt,
                               float* __restrict s, int Dp, int rows) {
   typedef typename Vec<W>::f vf;
+  typedef typename Vec<4>::f v4;
   constexpr int NV = CJ / W;
   for (int r0 = 0; r0 < rows; r0 += RB) {
     const float* q0 = q + (size_t)r0 * Dp;
@@ -178,13 +182,27 @@ HOST_INLINE void block_scores(const float* __restrict q, const float* __restrict
       vf acc[RB][NV];
       for (int rr = 0; rr < RB; ++rr)
         for (int t = 0; t < NV; ++t) acc[rr][t] = vf{};
-      const float* kc = kt + j0;
-      for (int c = 0; c < Dp; ++c, kc += BK) {
-        vf kv[NV];
-        for (int t = 0; t < NV; ++t) kv[t] = vload<W>(kc + t * W);
-        for (int rr = 0; rr < RB; ++rr) {
-          const float a = q0[(size_t)rr * Dp + c];
-          for (int t = 0; t < NV; ++t) acc[rr][t] = a * kv[t] + acc[rr][t];
+      if (LANES) {  // Dp is a multiple of CJ, hence of 4
+        for (int c = 0; c < Dp; c += 4) {
+          v4 qv[RB];
+          for (int rr = 0; rr < RB; ++rr) qv[rr] = vload<4>(q0 + (size_t)rr * Dp + c);
+          for (int cc = 0; cc < 4; ++cc) {
+            const float* kc = kt + (size_t)(c + cc) * BK + j0;
+            vf kv[NV];
+            for (int t = 0; t < NV; ++t) kv[t] = vload<W>(kc + t * W);
+            for (int rr = 0; rr < RB; ++rr)
+              for (int t = 0; t < NV; ++t) acc[rr][t] = kv[t] * qv[rr][cc] + acc[rr][t];
+          }
+        }
+      } else {
+        const float* kc = kt + j0;
+        for (int c = 0; c < Dp; ++c, kc += BK) {
+          vf kv[NV];
+          for (int t = 0; t < NV; ++t) kv[t] = vload<W>(kc + t * W);
+          for (int rr = 0; rr < RB; ++rr) {
+            const float a = q0[(size_t)rr * Dp + c];
+            for (int t = 0; t < NV; ++t) acc[rr][t] = a * kv[t] + acc[rr][t];
+          }
         }
       }
       for (int rr = 0; rr < RB; ++rr)
@@ -193,12 +211,14 @@ HOST_INLINE void block_scores(const float* __restrict q, const float* __restrict
   }
 }
 
-// o[r] = alpha[r] o[r] + sum_jj p[r][jj] vp[jj], for RB rows and one chunk of columns at a time
-template <int W, int RB>
+// o[r] = alpha[r] o[r] + sum_jj p[r][jj] vp[jj], for RB rows and one chunk of
+// columns at a time; LANES as in block_scores, over four consecutive p values
+template <int W, int RB, bool LANES>
 HOST_INLINE void block_accumulate(const float* __restrict p, const float* __restrict vp,
                                   float* __restrict o, const float* __restrict alpha, int Dp,
                                   int rows) {
   typedef typename Vec<W>::f vf;
+  typedef typename Vec<4>::f v4;
   constexpr int NV = CJ / W;
   for (int r0 = 0; r0 < rows; r0 += RB) {
     const float* p0 = p + (size_t)r0 * BK;
@@ -208,13 +228,27 @@ HOST_INLINE void block_accumulate(const float* __restrict p, const float* __rest
         const float a = alpha[r0 + rr];
         for (int t = 0; t < NV; ++t) acc[rr][t] = vload<W>(o + (size_t)(r0 + rr) * Dp + c0 + t * W) * a;
       }
-      const float* vr = vp + c0;
-      for (int jj = 0; jj < BK; ++jj, vr += Dp) {
-        vf vv[NV];
-        for (int t = 0; t < NV; ++t) vv[t] = vload<W>(vr + t * W);
-        for (int rr = 0; rr < RB; ++rr) {
-          const float pv = p0[(size_t)rr * BK + jj];
-          for (int t = 0; t < NV; ++t) acc[rr][t] = pv * vv[t] + acc[rr][t];
+      if (LANES) {
+        for (int jj = 0; jj < BK; jj += 4) {
+          v4 pv[RB];
+          for (int rr = 0; rr < RB; ++rr) pv[rr] = vload<4>(p0 + (size_t)rr * BK + jj);
+          for (int j2 = 0; j2 < 4; ++j2) {
+            const float* vr = vp + (size_t)(jj + j2) * Dp + c0;
+            vf vv[NV];
+            for (int t = 0; t < NV; ++t) vv[t] = vload<W>(vr + t * W);
+            for (int rr = 0; rr < RB; ++rr)
+              for (int t = 0; t < NV; ++t) acc[rr][t] = vv[t] * pv[rr][j2] + acc[rr][t];
+          }
+        }
+      } else {
+        const float* vr = vp + c0;
+        for (int jj = 0; jj < BK; ++jj, vr += Dp) {
+          vf vv[NV];
+          for (int t = 0; t < NV; ++t) vv[t] = vload<W>(vr + t * W);
+          for (int rr = 0; rr < RB; ++rr) {
+            const float pv = p0[(size_t)rr * BK + jj];
+            for (int t = 0; t < NV; ++t) acc[rr][t] = pv * vv[t] + acc[rr][t];
+          }
         }
       }
       for (int rr = 0; rr < RB; ++rr)
@@ -257,7 +291,7 @@ HOST_INLINE void row_update(float* __restrict sr, float& m, float& l, float& alp
   m = m_new;
 }
 
-template <int W, int RB>
+template <int W, int RB, bool LANES>
 HOST_INLINE void run_task_w(const Problem& pr, Scratch& sc, long long bh, int qt) {
   const int d = pr.d, Dp = pr.Dp, N = pr.N;
   const int i0 = qt * BQ, rows = std::min(BQ, N - i0);
@@ -278,7 +312,7 @@ HOST_INLINE void run_task_w(const Problem& pr, Scratch& sc, long long bh, int qt
   for (int kb = 0; kb < kb_end; ++kb) {
     const int j0 = kb * BK;
     const size_t blk = ((size_t)bh * pr.nkb + kb) * (size_t)Dp * BK;
-    block_scores<W, RB>(sc.q, pr.kt + blk, sc.s, Dp, rows_p);
+    block_scores<W, RB, LANES>(sc.q, pr.kt + blk, sc.s, Dp, rows_p);
     // masks before the block max: keys past N, and (causal) keys after the query
     const bool ragged = j0 + BK > N;
     const bool diag = pr.causal && j0 + BK - 1 > i0;
@@ -297,7 +331,7 @@ HOST_INLINE void run_task_w(const Problem& pr, Scratch& sc, long long bh, int qt
         for (int jj = 0; jj < BK; ++jj) sc.s[(size_t)r * BK + jj] = 0.f;
       }
     }
-    block_accumulate<W, RB>(sc.s, pr.vp + blk, sc.o, sc.alpha, Dp, rows_p);
+    block_accumulate<W, RB, LANES>(sc.s, pr.vp + blk, sc.o, sc.alpha, Dp, rows_p);
   }
   // O = o~ / l;  LSE = m + ln l, back from base-2 units
   float* og = pr.o + ((size_t)bh * N + i0) * d;
@@ -317,9 +351,11 @@ HOST_INLINE float fma_loop_w(long long iters, float a, float b) {
   vf acc[KV];
   for (int u = 0; u < KV; ++u) acc[u] = vsplat<W>((float)u * 1e-3f);
   const vf va = vsplat<W>(a), vb = vsplat<W>(b);
+  // the running value is the addend (acc += va * vb), the form the kernels use:
+  // a multiply-add that accumulates into its destination register
   for (long long it = 0; it < iters; ++it)
 #pragma GCC unroll 16
-    for (int u = 0; u < KV; ++u) acc[u] = acc[u] * va + vb;
+    for (int u = 0; u < KV; ++u) acc[u] = va * vb + acc[u];
   // whole-vector adds, then the lanes of one vector (indexing the array by a
   // run-time lane would keep it in memory through the loop above)
   vf t = acc[0];
@@ -352,9 +388,9 @@ struct Kernels {
   int flops_per_iter;  // 2 * KV * W
 };
 
-#define DEFINE_KERNELS(NAME, TARGET, W, RB, KV)                                          \
+#define DEFINE_KERNELS(NAME, TARGET, W, RB, LANES, KV)                                   \
   TARGET void NAME##_run(const Problem& pr, Scratch& sc, long long bh, int qt) {         \
-    run_task_w<W, RB>(pr, sc, bh, qt);                                                   \
+    run_task_w<W, RB, LANES>(pr, sc, bh, qt);                                            \
   }                                                                                      \
   TARGET float NAME##_fma(long long it, float a, float b) {                              \
     return fma_loop_w<W, KV>(it, a, b);                                                  \
@@ -364,9 +400,9 @@ struct Kernels {
 
 #if defined(__x86_64__) && defined(__GNUC__) && !defined(__clang__)
 // AVX-512 (32 registers of 16 floats), AVX2 + FMA (16 of 8), SSE (16 of 4)
-DEFINE_KERNELS(k_avx512, __attribute__((target("arch=x86-64-v4"))), 16, 8, 8)
-DEFINE_KERNELS(k_avx2, __attribute__((target("arch=x86-64-v3"))), 8, 4, 8)
-DEFINE_KERNELS(k_sse, , 4, 2, 8)
+DEFINE_KERNELS(k_avx512, __attribute__((target("arch=x86-64-v4"))), 16, 8, false, 8)
+DEFINE_KERNELS(k_avx2, __attribute__((target("arch=x86-64-v3"))), 8, 4, false, 8)
+DEFINE_KERNELS(k_sse, , 4, 2, false, 8)
 const Kernels& kernels() {
   static const Kernels* k = [] {
     __builtin_cpu_init();
@@ -378,7 +414,7 @@ const Kernels& kernels() {
 }
 #else
 // AArch64 NEON: 32 registers of 4 floats, four FMA pipes of four-cycle latency
-DEFINE_KERNELS(k_neon, , 4, 4, 16)
+DEFINE_KERNELS(k_neon, , 4, 4, true, 16)
 const Kernels& kernels() { return k_neon; }
 #endif
 

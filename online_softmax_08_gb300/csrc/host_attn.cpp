@@ -176,21 +176,28 @@ HOST_INLINE void block_scores(const float* __restrict q, const float* __restrict
   typedef typename Vec<W>::f vf;
   typedef typename Vec<4>::f v4;
   constexpr int NV = CJ / W;
-  for (int r0 = 0; r0 < rows; r0 += RB) {
-    const float* q0 = q + (size_t)r0 * Dp;
-    for (int j0 = 0; j0 < BK; j0 += CJ) {
+  for (int j0 = 0; j0 < BK; j0 += CJ) {  // this chunk's K strip stays in L1 across row blocks
+    for (int r0 = 0; r0 < rows; r0 += RB) {
+      const float* q0 = q + (size_t)r0 * Dp;
       vf acc[RB][NV];
+#pragma GCC unroll 16
       for (int rr = 0; rr < RB; ++rr)
+#pragma GCC unroll 16
         for (int t = 0; t < NV; ++t) acc[rr][t] = vf{};
       if (LANES) {  // Dp is a multiple of CJ, hence of 4
         for (int c = 0; c < Dp; c += 4) {
           v4 qv[RB];
+#pragma GCC unroll 16
           for (int rr = 0; rr < RB; ++rr) qv[rr] = vload<4>(q0 + (size_t)rr * Dp + c);
+#pragma GCC unroll 16
           for (int cc = 0; cc < 4; ++cc) {
             const float* kc = kt + (size_t)(c + cc) * BK + j0;
             vf kv[NV];
+#pragma GCC unroll 16
             for (int t = 0; t < NV; ++t) kv[t] = vload<W>(kc + t * W);
+#pragma GCC unroll 16
             for (int rr = 0; rr < RB; ++rr)
+#pragma GCC unroll 16
               for (int t = 0; t < NV; ++t) acc[rr][t] = kv[t] * qv[rr][cc] + acc[rr][t];
           }
         }
@@ -198,14 +205,19 @@ HOST_INLINE void block_scores(const float* __restrict q, const float* __restrict
         const float* kc = kt + j0;
         for (int c = 0; c < Dp; ++c, kc += BK) {
           vf kv[NV];
+#pragma GCC unroll 16
           for (int t = 0; t < NV; ++t) kv[t] = vload<W>(kc + t * W);
+#pragma GCC unroll 16
           for (int rr = 0; rr < RB; ++rr) {
             const float a = q0[(size_t)rr * Dp + c];
+#pragma GCC unroll 16
             for (int t = 0; t < NV; ++t) acc[rr][t] = a * kv[t] + acc[rr][t];
           }
         }
       }
+#pragma GCC unroll 16
       for (int rr = 0; rr < RB; ++rr)
+#pragma GCC unroll 16
         for (int t = 0; t < NV; ++t) vstore<W>(s + (size_t)(r0 + rr) * BK + j0 + t * W, acc[rr][t]);
     }
   }
@@ -220,23 +232,30 @@ HOST_INLINE void block_accumulate(const float* __restrict p, const float* __rest
   typedef typename Vec<W>::f vf;
   typedef typename Vec<4>::f v4;
   constexpr int NV = CJ / W;
-  for (int r0 = 0; r0 < rows; r0 += RB) {
-    const float* p0 = p + (size_t)r0 * BK;
-    for (int c0 = 0; c0 < Dp; c0 += CJ) {
+  for (int c0 = 0; c0 < Dp; c0 += CJ) {  // this chunk's V strip stays in L1 across row blocks
+    for (int r0 = 0; r0 < rows; r0 += RB) {
+      const float* p0 = p + (size_t)r0 * BK;
       vf acc[RB][NV];
+#pragma GCC unroll 16
       for (int rr = 0; rr < RB; ++rr) {
         const float a = alpha[r0 + rr];
+#pragma GCC unroll 16
         for (int t = 0; t < NV; ++t) acc[rr][t] = vload<W>(o + (size_t)(r0 + rr) * Dp + c0 + t * W) * a;
       }
       if (LANES) {
         for (int jj = 0; jj < BK; jj += 4) {
           v4 pv[RB];
+#pragma GCC unroll 16
           for (int rr = 0; rr < RB; ++rr) pv[rr] = vload<4>(p0 + (size_t)rr * BK + jj);
+#pragma GCC unroll 16
           for (int j2 = 0; j2 < 4; ++j2) {
             const float* vr = vp + (size_t)(jj + j2) * Dp + c0;
             vf vv[NV];
+#pragma GCC unroll 16
             for (int t = 0; t < NV; ++t) vv[t] = vload<W>(vr + t * W);
+#pragma GCC unroll 16
             for (int rr = 0; rr < RB; ++rr)
+#pragma GCC unroll 16
               for (int t = 0; t < NV; ++t) acc[rr][t] = vv[t] * pv[rr][j2] + acc[rr][t];
           }
         }
@@ -244,14 +263,19 @@ HOST_INLINE void block_accumulate(const float* __restrict p, const float* __rest
         const float* vr = vp + c0;
         for (int jj = 0; jj < BK; ++jj, vr += Dp) {
           vf vv[NV];
+#pragma GCC unroll 16
           for (int t = 0; t < NV; ++t) vv[t] = vload<W>(vr + t * W);
+#pragma GCC unroll 16
           for (int rr = 0; rr < RB; ++rr) {
             const float pv = p0[(size_t)rr * BK + jj];
+#pragma GCC unroll 16
             for (int t = 0; t < NV; ++t) acc[rr][t] = pv * vv[t] + acc[rr][t];
           }
         }
       }
+#pragma GCC unroll 16
       for (int rr = 0; rr < RB; ++rr)
+#pragma GCC unroll 16
         for (int t = 0; t < NV; ++t) vstore<W>(o + (size_t)(r0 + rr) * Dp + c0 + t * W, acc[rr][t]);
     }
   }
@@ -414,7 +438,7 @@ const Kernels& kernels() {
 }
 #else
 // AArch64 NEON: 32 registers of 4 floats, four FMA pipes of four-cycle latency
-DEFINE_KERNELS(k_neon, , 4, 4, true, 16)
+DEFINE_KERNELS(k_neon, , 4, 4, false, 16)
 const Kernels& kernels() { return k_neon; }
 #endif
 

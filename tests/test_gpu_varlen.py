@@ -26,6 +26,10 @@ CASES = [
     ([777, 0, 64, 1000], 2, 64, True),
     ([256, 256, 256], 3, 64, False),
     ([5, 1300, 3], 1, 128, True),
+    # equal lengths among others: CTAs take sequences longest first, ties by index
+    ([300, 200, 300, 128, 0, 300, 256, 700], 2, 128, True),
+    # more sequences than the longest-first ordering handles: index order
+    ([(37 * i) % 301 for i in range(70)], 1, 64, True),
 ]
 
 

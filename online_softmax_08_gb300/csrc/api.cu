@@ -5,6 +5,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/fattn.h"
@@ -92,6 +93,9 @@ int check_common(int B, int H, int N, int d, float scale) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Share of the 129 MB L2 that the CTAs in flight of the dense kernels may read from.
+constexpr long long kL2GroupBytes = 32LL << 20;
+
 }  // namespace
 }  // namespace fattn
 
@@ -135,6 +139,8 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
   p.err = dev->err;
   p.vl = g.vl;
   p.o = static_cast<uint16_t*>(o);
+  // dense: groups of heads whose K and V (4 N d bytes a head) fit in 32 MiB of L2
+  p.group = (int)std::max<long long>(1, (kL2GroupBytes) / (4LL * g.N * d));
   cudaError_t e = launch_fwd(d, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
@@ -194,6 +200,9 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const fl
   p.vl = g.vl;
   p.dk = static_cast<uint16_t*>(dk);
   p.dv = static_cast<uint16_t*>(dv);
+  // dense: groups of heads whose Q, dO (bf16) and dQ accumulator (fp32), 8 N d
+  // bytes a head, fit in 32 MiB of L2
+  p.group = (int)std::max<long long>(1, (kL2GroupBytes) / (8LL * g.N * d));
   cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, tdk, tdv, tdq, p, s);
   if (e == cudaErrorNotSupported) return FATTN_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return FATTN_ERR_CUDA;

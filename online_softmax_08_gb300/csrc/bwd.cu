@@ -162,13 +162,19 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
   uint8_t* smem = smem_raw + (sbase - raw);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // key block kb (causal: heaviest first).  Dense: key-block-major; varlen: one
+  // key block kb (causal: heaviest first).  Dense: key-block-major within groups
+  // of heads; varlen: one
   // (sequence, head) unit after another, so the CTAs in flight share their
   // unit's Q, dO and dQ accumulator in L2
   const int units = VARLEN ? p.vl.B * p.vl.H : p.BH;
   const int n_kb_grid = (p.N + C::BK - 1) / C::BK;
-  const int kb = VARLEN ? (int)(blockIdx.x % (unsigned)n_kb_grid) : (int)(blockIdx.x / (unsigned)units);
-  const int unit = VARLEN ? (int)(blockIdx.x / (unsigned)n_kb_grid) : (int)(blockIdx.x % (unsigned)units);
+  int kb, unit;
+  if (VARLEN) {
+    kb = (int)(blockIdx.x % (unsigned)n_kb_grid);
+    unit = (int)(blockIdx.x / (unsigned)n_kb_grid);
+  } else {  // heads in groups whose Q, dO and dQ accumulator stay in L2 (p.group)
+    grouped_order(blockIdx.x, units, n_kb_grid, p.group, &kb, &unit);
+  }
   SeqView seq;
   if constexpr (VARLEN) {
     if (!seq_view(p.vl, p.N, unit / p.vl.H, unit % p.vl.H, unit, p.N, &seq)) {

@@ -43,6 +43,7 @@ struct FwdParams {
   int tiles_per_split;
   float* o_part;
   float* lse_part;
+  int group;                  // dense grid: heads per group of the CTA order (0: one group)
 };
 
 struct BwdParams {
@@ -58,7 +59,26 @@ struct BwdParams {
   Varlen vl;
   uint16_t* dk;               // dK, dV (bf16 bits); varlen writes the last key block of a
   uint16_t* dv;               // sequence row by row
+  int group;                  // dense grid: heads per group of the CTA order (0: one group)
 };
+
+// Dense grid order: the CTAs go through the heads in groups of `group` heads
+// and, within a group, block by block (all of the group's heads for block 0,
+// then block 1, ...), so the CTAs in flight read the tensors of one or two
+// groups, which stay in L2.  group = 0 (or >= units) is one group: the order
+// is block-major over all heads.  Returns the CTA's block index in that order
+// and its (b, h) unit.
+__device__ __forceinline__ void grouped_order(unsigned bidx, int units, int blocks, int group,
+                                              int* blk, int* unit) {
+  const int G = (group > 0 && group < units) ? group : units;
+  const unsigned per_group = (unsigned)blocks * (unsigned)G;
+  const int g = (int)(bidx / per_group);
+  const int first = g * G;
+  const int gs = min(G, units - first);  // only the last group may be smaller
+  const unsigned r = bidx - (unsigned)g * per_group;
+  *blk = (int)(r / (unsigned)gs);
+  *unit = first + (int)(r % (unsigned)gs);
+}
 
 // Where a CTA's sequence lives: its length, its first row in the tensor's
 // row dimension, the TMA z coordinate (b*H + h dense, h varlen), and the base

@@ -129,13 +129,19 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
   const unsigned bidx = SPLIT ? blockIdx.x / (unsigned)p.n_splits : blockIdx.x;
   const int n_qb = ((SPLIT ? p.Nq : p.N) + 255) / 256;  // p.N: the (longest) sequence length
   // heaviest (last) query blocks first
-  // dense: query-block-major, so the CTAs in flight cover every (b, h); varlen:
+  // dense: query-block-major within groups of heads; varlen:
   // one (sequence, head) unit after another, so the CTAs in flight share their
   // unit's K/V in L2 (a unit-spread order streams each CTA's K/V from DRAM)
   const int units = VARLEN ? p.vl.B * p.vl.H : p.BH;
-  const int qb = VARLEN ? n_qb - 1 - (int)(bidx % (unsigned)n_qb)
-                        : n_qb - 1 - (int)(bidx / (unsigned)units);
-  const int unit = VARLEN ? (int)(bidx / (unsigned)n_qb) : (int)(bidx % (unsigned)units);
+  int qb, unit;
+  if (VARLEN) {
+    qb = n_qb - 1 - (int)(bidx % (unsigned)n_qb);
+    unit = (int)(bidx / (unsigned)n_qb);
+  } else {  // heads in groups whose K/V stay in L2 (p.group)
+    int blk;
+    grouped_order(bidx, units, n_qb, p.group, &blk, &unit);
+    qb = n_qb - 1 - blk;
+  }
   SeqView seq;
   if constexpr (VARLEN) {
     if (!seq_view(p.vl, p.N, unit / p.vl.H, unit % p.vl.H, unit, p.N, &seq)) {

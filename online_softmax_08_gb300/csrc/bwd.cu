@@ -25,11 +25,12 @@
 // is overwritten in place by the bf16 P^T, and a region Y that holds dP^T until
 // dS is formed and then dQ^T.  The MMA warp issues, per step i,
 //
-//   dP(i) -> Y  dV(i)  S(i+1) -> X  dK(i)  dQ(i) -> Y
+//   dP(i) -> Y  dV(i)  S(i+1) -> X  dK(i) (first half)  dK(i) (second half)  dQ(i) -> Y
 //
 // dP(i) does not wait for P(i), so dS(i) starts as soon as it lands; dV(i) and
-// S(i+1) execute while dS(i) is formed, and P(i+1) is formed while dK(i),
-// dQ(i) and the next dP execute.  Each compute warpgroup keeps the bf16 P^T
+// S(i+1) execute while dS(i) is formed, and so does the half of dK(i) over the
+// queries of the compute warps' first pass.  P(i+1) is formed while the rest
+// of dK(i), dQ(i) and the next dP execute.  Each compute warpgroup keeps the bf16 P^T
 // of its 64 queries in registers from P to dS, so X can take S(i+1) right
 // after dV(i).  The dQ^T partial of each
 // step is read out of TMEM by a drain warpgroup (freeing Y for dP(i+1)) and
@@ -92,6 +93,7 @@ enum {
   B_KV = 0,
   B_S_FULL = 1,     // MMA -> compute warps: S^T in X
   B_P_FULL = 2,     // compute warps -> MMA: P^T (bf16) in X, S^T read
+  B_DS_HALF = 3,    // compute warps -> MMA: the first 32 queries of each half of dS^T stored
   B_DP_FULL = 4,    // MMA -> compute warps: dP^T in Y
   B_DS_FULL = 5,    // compute warps -> MMA: dS^T in shared memory, dP^T read
   B_DS_FREE = 6,    // MMA -> compute warps: dK and dQ have read dS^T
@@ -204,6 +206,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
     mbar_init(bar(B_S_FULL), 1);
     mbar_init(bar(B_P_FULL), 256);
     mbar_init(bar(B_DP_FULL), 1);
+    mbar_init(bar(B_DS_HALF), 256);
     mbar_init(bar(B_DS_FULL), 256);
     mbar_init(bar(B_DS_FREE), 1);
     mbar_init(bar(B_DQ_FULL), 1);
@@ -319,10 +322,13 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
                         sdesc_sw128(sdo + kk * 16 * 128, C::HALF, 1024), C::IDESC_ACC,
                         (acc || kk > 0));
       };
-      // dK += dS^T (K-major) * Q (MN-major)
-      auto mma_dk = [&](uint32_t sq, bool acc) {
+      // dK += dS^T (K-major) * Q (MN-major), over the 16-query steps kk of one
+      // pass: pass 0 takes queries 0-31 of each 64-query half (kk = 0, 1, 4, 5),
+      // pass 1 queries 32-63 (kk = 2, 3, 6, 7), as the compute warps store them
+      auto mma_dk = [&](uint32_t sq, bool acc, int pass) {
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {
+        for (int j = 0; j < BQ / 32; ++j) {
+          const int kk = (j >> 1) * 4 + pass * 2 + (j & 1);
           const uint32_t ao = (kk >> 2) * C::HALF + (kk & 3) * 32;
           mma_bf16_ss_w(tmem + C::TM_DK, sdesc_sw128(sDS + ao, 16, 1024),
                         sdesc_sw128(sq + kk * 16 * 128, C::HALF, 1024), C::IDESC_ACC,
@@ -373,10 +379,14 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
           mma_xyT(C::TM_X, sK, sQ(it + 1));
           mma_commit_w(bar(B_S_FULL));
         }
-        // dK(i), dQ(i) once dS^T(i) is in shared memory
+        // dK(i) over the queries of the compute warps' first pass while they do
+        // the second, then the rest of dK(i) and dQ(i) once dS^T(i) is complete
+        if (!(ok = wait_all(B_DS_HALF, it, 0x19))) break;
+        tc_fence_after();
+        mma_dk(sQ(it), it > 0, 0);
         if (!(ok = wait_all(B_DS_FULL, it, 0x15))) break;
         tc_fence_after();
-        mma_dk(sQ(it), it > 0);
+        mma_dk(sQ(it), true, 1);
         mma_commit_w(bar(B_Q_EMPTY + it % QST));  // dK is the last reader of Q(i)
         mma_dq();
         mma_commit_w(bar(B_DQ_FULL));
@@ -538,6 +548,10 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
                        pack_bf16x2(ds[e * 8 + 2], ds[e * 8 + 3]),
                        pack_bf16x2(ds[e * 8 + 4], ds[e * 8 + 5]),
                        pack_bf16x2(ds[e * 8 + 6], ds[e * 8 + 7]));
+        }
+        if (c == 0) {  // the first pass's dS^T is in shared memory: dK can start on it
+          fence_proxy_async_smem();
+          mbar_arrive(bar(B_DS_HALF));
         }
       }
       mbar_arrive(bar(B_Q_EMPTY + st));  // LSE2 and D of this stage are no longer read

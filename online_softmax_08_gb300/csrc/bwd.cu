@@ -35,9 +35,10 @@
 // after dV(i).  The dQ^T partial of each
 // step is read out of TMEM by a drain warpgroup (freeing Y for dP(i+1)) and
 // added into an fp32 accumulator with bulk tensor reduces of 16 query rows,
-// staged through two shared-memory buffers so that filling one overlaps the
-// reduce reading the other (measured 11 % faster for the whole kernel than one
-// buffer).  The alternative, a second pass parallel over query blocks, would
+// staged round-robin through NDQ shared-memory buffers so that filling one
+// overlaps the reduces reading the others (two buffers were 11 % faster than
+// one, three 1.2 % faster than two); the drain is busy for the whole step, so
+// these reductions are what bounds the kernel.  The alternative, a second pass parallel over query blocks, would
 // recompute S and dP (seven matmuls per tile instead of five).
 //
 // Warp roles (512 threads): warps 0-7 form P and dS, warpgroup w for queries
@@ -67,8 +68,11 @@ struct Bwd {
   static constexpr int OFF_DO = OFF_Q + QST * TILE;            // [OST]
   static constexpr int OFF_DS = OFF_DO + OST * TILE;           // dS^T [128 keys][128 q] bf16
   static constexpr int OFF_STAT = OFF_DS + 2 * HALF;           // [QST] x {-lse2[BQ], delta[BQ]}
-  static constexpr int OFF_DQ = OFF_STAT + QST * 2 * BQ * 4;  // fp32 staging [2][16 q][D]
-  static constexpr int OFF_BAR = OFF_DQ + 2 * 16 * D * 4;
+  // dQ staging: NDQ buffers of 16 query rows (fp32), filled round-robin, so that
+  // NDQ - 1 bulk reduces are in flight while the next buffer is filled
+  static constexpr int NDQ = D == 128 ? 3 : 4;
+  static constexpr int OFF_DQ = OFF_STAT + QST * 2 * BQ * 4;  // fp32 staging [NDQ][16 q][D]
+  static constexpr int OFF_BAR = OFF_DQ + NDQ * 16 * D * 4;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   static constexpr int THREADS = 512;
   static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_X = 2 * D, TM_Y = 2 * D + 128;
@@ -403,6 +407,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
     const int t = threadIdx.x & 127;  // TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t sdq = sbase + C::OFF_DQ;
+    int nbuf = 0;  // chunks staged so far: the buffer of the next one is nbuf % NDQ
     for (int it = 0; it < n_it; ++it) {
       const int q0 = (i_start + it) * BQ;
       mbar_wait(bar(B_DQ_FULL), it & 1, wctx, ERR_SITE_BWD | 0x31);
@@ -418,10 +423,10 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
       // lanes are d (lanes >= d are padding), columns are queries: stage 16 query
       // rows at a time in shared memory and add them with one bulk tensor reduce
 #pragma unroll
-      for (int h = 0; h < 8; ++h) {  // 16 query rows per reduce, two staging buffers
-        const uint32_t buf = sdq + (uint32_t)(h & 1) * (16 * D * 4);
-        // the reduce issued two chunks ago (same buffer) has read it
-        if (t == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      for (int h = 0; h < 8; ++h, ++nbuf) {  // 16 query rows per reduce
+        const uint32_t buf = sdq + (uint32_t)(nbuf % C::NDQ) * (16 * D * 4);
+        // the reduce that last read this buffer, NDQ chunks ago, is done reading it
+        if (t == 0) bulk_wait_read<C::NDQ - 1>();
         named_bar_sync(2, 128);
         if (t < D) {
 #pragma unroll

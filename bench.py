@@ -345,6 +345,18 @@ def run_gpu(args):
                 else None,
                 "algorithmic_bytes": fwd_bytes}
 
+    # the forward's second ceiling: one exponential per visible score against the
+    # measured ex2 rate of this GPU
+    roof_exp = None
+    if do_fwd:
+        visible = B * H * (N * (N + 1) / 2.0 if causal else float(N) * N)
+        ex2_peak = fattn.ex2_throughput() / 1e12
+        exps = visible / (fwd_ms * 1e-3) / 1e12
+        roof_exp = {"kernel": "fattn_fwd_kernel<%d>" % d, "bound": "mufu", "achieved": exps,
+                    "peak": ex2_peak, "unit": "Texp/s", "frac": exps / ex2_peak,
+                    "peak_source": "measured (fattn_ex2_throughput)",
+                    "algorithmic_exps": visible}
+
     # end to end through the C-ABI with host buffers: fattn_fwd_bwd_host copies
     # Q, K, V, dO in from pinned host memory, runs the forward and the backward
     # and copies O, LSE, dQ, dK, dV back, chunk by chunk of heads with the copies
@@ -405,7 +417,7 @@ def run_gpu(args):
             "bwd": {"ms": pre_ms + main_ms + conv_ms, "preprocess_ms": pre_ms,
                     "main_ms": main_ms, "convert_ms": conv_ms,
                     "tflops": f_bwd / ((pre_ms + main_ms + conv_ms) * 1e-3) / 1e12},
-            "roofline": roof, "roofline_fwd": roof_fwd,
+            "roofline": roof, "roofline_fwd": roof_fwd, "roofline_fwd_exp": roof_exp,
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": (int(do_fwd) + 3 * int(do_bwd)) * K,
             "clocks": clk,

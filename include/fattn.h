@@ -249,6 +249,14 @@ int fattn_device_error(unsigned int* code, int clear);
  * counterpart; it tests this library's own timeout reporting. */
 int fattn_check_wait_timeout(void* stream);
 
+/* Measured throughput of the exponential unit of the current device, in ex2
+ * evaluations per second: a kernel of independent ex2.approx chains on every
+ * SM, timed with events on `stream` (a warm-up launch, then one timed launch;
+ * the call synchronises with the timed launch).  It is the second ceiling of
+ * the forward pass, which takes one exponential per visible score.  Returns
+ * FATTN_OK, FATTN_ERR_INVALID_ARG (per_second NULL) or FATTN_ERR_CUDA. */
+int fattn_ex2_throughput(double* per_second, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* fattn_status_string(int status);
 

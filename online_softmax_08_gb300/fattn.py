@@ -48,6 +48,7 @@ SIGNATURES = {
     "fattn_fwd_bwd_host_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "fattn_fwd_bwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f,
                                 _i, _i, _vp, _sz, _vp]),
+    "fattn_ex2_throughput": (_i, [ctypes.POINTER(ctypes.c_double), _vp]),
     "fattn_status_string": (ctypes.c_char_p, [_i]),
 }
 
@@ -197,6 +198,13 @@ def check_wait_timeout(stream=None):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream().cuda_stream
     _check("fattn_check_wait_timeout", load().fattn_check_wait_timeout(s))
+
+
+def ex2_throughput(stream=None):
+    """Measured ex2 evaluations per second of the current device (synchronises)."""
+    rate = ctypes.c_double(0.0)
+    _check("fattn_ex2_throughput", load().fattn_ex2_throughput(ctypes.byref(rate), _stream(stream)))
+    return rate.value
 
 
 def fattn_status_string(status):

@@ -84,6 +84,10 @@ def test_argument_checks_before_any_device_call(lib):
     assert lib.fattn_bwd(a, a, a, a, a, a, a, a, a, 1, 1, 128, 128, 0.1, 1, a, 16, None) == 4
 
 
+def test_ex2_probe_checks_its_pointer_first(lib):
+    assert lib.fattn_ex2_throughput(None, None) == 1
+
+
 def test_host_staged_argument_checks_before_any_device_call(lib):
     a = 1 << 20
     ws = 1 << 24  # 256-byte aligned, never dereferenced

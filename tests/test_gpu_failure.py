@@ -48,3 +48,11 @@ def test_first_failure_wins():
     assert fattn.fattn_device_error(clear=False) == CHECK_SITE
     assert fattn.fattn_device_error(clear=True) == CHECK_SITE
     assert fattn.fattn_device_error() == 0
+
+
+def test_ex2_throughput_probe_is_plausible():
+    """The measured ex2 rate (the forward pass's second ceiling) lies between
+    1e12/s and 2e13/s on a GB300 (16 per clock per SM x 152 SMs x about 2 GHz
+    is about 5e12/s)."""
+    rate = fattn.ex2_throughput()
+    assert 1e12 < rate < 2e13, rate

@@ -254,6 +254,10 @@ def run_gpu(args):
 
     w = WORKLOADS[args.workload]
     B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"][-1]
+    if args.causal != "default":  # profiling: another masking mode the workload lists
+        causal = args.causal == "yes"
+        if causal not in w["causal"]:
+            raise SystemExit("workload %s has no %s mode" % (args.workload, args.causal))
     scale = default_scale(d)
     f_fwd, f_bwd = flops(B, H, N, d, causal)
     do_fwd, do_bwd = args.passes in ("both", "fwd"), args.passes in ("both", "bwd")
@@ -705,6 +709,8 @@ def main(argv=None):
     ap.add_argument("--pass", dest="passes", default="both", choices=["both", "fwd", "bwd"],
                     help="profiling only: time one pass; a benchmark step is both")
     ap.add_argument("--splits", default=0, help="decode workloads: key ranges (0 = automatic)")
+    ap.add_argument("--causal", default="default", choices=["default", "yes", "no"],
+                    help="profiling only: the masking mode of a fixed-shape workload")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-chunk", default=0,
                     help="heads per chunk of the end-to-end leg (0 = the library's choice)")

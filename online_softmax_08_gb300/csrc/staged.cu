@@ -159,60 +159,73 @@ extern "C" int fattn_fwd_bwd_host(const void* q, const void* k, const void* v, c
       !ok(cudaStreamWaitEvent(p->s_out, p->start, 0)))
     return FATTN_ERR_CUDA;
 
-  const long long BH = (long long)B * H;
-  const size_t head_bytes = (size_t)N * d * 2;
-  const void* in_host[4] = {q, k, v, dout};
-  void* out_host[4] = {o, dq, dk, dv};
-  const int first = (heads + 1) / 2;
-  long long c = 0;
-  for (long long h0 = 0; h0 < BH; ++c) {
-    const int s = (int)(c % kSlots);
-    const long long want = c == 0 ? first : heads;
-    const int hc = (int)((BH - h0) < want ? (BH - h0) : want);
-    char* slot = static_cast<char*>(workspace) + (size_t)s * L.bytes;
-    char* dev[8];  // q k v do o dq dk dv
-    for (int i = 0; i < 8; ++i) dev[i] = slot + L.off(i);
-    float* dlse = reinterpret_cast<float*>(slot + L.off_lse());
-    void* ws = slot + L.off_ws();
-    const size_t bytes = (size_t)hc * head_bytes;
-    const size_t host_off = (size_t)h0 * head_bytes;
-    auto copy_in = [&](int i) {
-      return ok(cudaMemcpyAsync(dev[i], static_cast<const char*>(in_host[i]) + host_off, bytes,
-                                cudaMemcpyHostToDevice, p->s_in));
-    };
-    auto copy_out = [&](int i) {  // i = 0..3: o dq dk dv
-      return ok(cudaMemcpyAsync(static_cast<char*>(out_host[i]) + host_off, dev[4 + i], bytes,
-                                cudaMemcpyDeviceToHost, p->s_out));
-    };
+  // every chunk's copies and kernels; returns the status of the first failure
+  long long n_chunks = 0;
+  auto enqueue_chunks = [&]() -> int {
+    const long long BH = (long long)B * H;
+    const size_t head_bytes = (size_t)N * d * 2;
+    const void* in_host[4] = {q, k, v, dout};
+    void* out_host[4] = {o, dq, dk, dv};
+    const int first = (heads + 1) / 2;
+    long long c = 0;
+    for (long long h0 = 0; h0 < BH; ++c) {
+      const int s = (int)(c % kSlots);
+      const long long want = c == 0 ? first : heads;
+      const int hc = (int)((BH - h0) < want ? (BH - h0) : want);
+      char* slot = static_cast<char*>(workspace) + (size_t)s * L.bytes;
+      char* dev[8];  // q k v do o dq dk dv
+      for (int i = 0; i < 8; ++i) dev[i] = slot + L.off(i);
+      float* dlse = reinterpret_cast<float*>(slot + L.off_lse());
+      void* ws = slot + L.off_ws();
+      const size_t bytes = (size_t)hc * head_bytes;
+      const size_t host_off = (size_t)h0 * head_bytes;
+      auto copy_in = [&](int i) {
+        return ok(cudaMemcpyAsync(dev[i], static_cast<const char*>(in_host[i]) + host_off, bytes,
+                                  cudaMemcpyHostToDevice, p->s_in));
+      };
+      auto copy_out = [&](int i) {  // i = 0..3: o dq dk dv
+        return ok(cudaMemcpyAsync(static_cast<char*>(out_host[i]) + host_off, dev[4 + i], bytes,
+                                  cudaMemcpyDeviceToHost, p->s_out));
+      };
 
-    // copy in (after the slot's previous contents have been copied out)
-    if (c >= kSlots && !ok(cudaStreamWaitEvent(p->s_in, p->out_done[s], 0))) return FATTN_ERR_CUDA;
-    if (!copy_in(0) || !copy_in(1) || !copy_in(2) || !ok(cudaEventRecord(p->qkv_in[s], p->s_in)) ||
-        !copy_in(3) || !ok(cudaEventRecord(p->do_in[s], p->s_in)))
-      return FATTN_ERR_CUDA;
+      // copy in (after the slot's previous contents have been copied out)
+      if (c >= kSlots && !ok(cudaStreamWaitEvent(p->s_in, p->out_done[s], 0))) return FATTN_ERR_CUDA;
+      if (!copy_in(0) || !copy_in(1) || !copy_in(2) || !ok(cudaEventRecord(p->qkv_in[s], p->s_in)) ||
+          !copy_in(3) || !ok(cudaEventRecord(p->do_in[s], p->s_in)))
+        return FATTN_ERR_CUDA;
 
-    // forward once Q, K, V are in; backward once dO is in too
-    if (!ok(cudaStreamWaitEvent(p->s_comp, p->qkv_in[s], 0))) return FATTN_ERR_CUDA;
-    st = fattn_fwd(dev[0], dev[1], dev[2], dev[4], dlse, 1, hc, N, d, scale, causal, p->s_comp);
-    if (st != FATTN_OK) return st;
-    if (!ok(cudaEventRecord(p->fwd_done[s], p->s_comp)) ||
-        !ok(cudaStreamWaitEvent(p->s_comp, p->do_in[s], 0)))
-      return FATTN_ERR_CUDA;
-    st = fattn_bwd(dev[0], dev[1], dev[2], dev[4], dlse, dev[3], dev[5], dev[6], dev[7], 1, hc, N,
-                   d, scale, causal, ws, L.bwd_ws, p->s_comp);
-    if (st != FATTN_OK) return st;
-    if (!ok(cudaEventRecord(p->bwd_done[s], p->s_comp))) return FATTN_ERR_CUDA;
+      // forward once Q, K, V are in; backward once dO is in too
+      if (!ok(cudaStreamWaitEvent(p->s_comp, p->qkv_in[s], 0))) return FATTN_ERR_CUDA;
+      st = fattn_fwd(dev[0], dev[1], dev[2], dev[4], dlse, 1, hc, N, d, scale, causal, p->s_comp);
+      if (st != FATTN_OK) return st;
+      if (!ok(cudaEventRecord(p->fwd_done[s], p->s_comp)) ||
+          !ok(cudaStreamWaitEvent(p->s_comp, p->do_in[s], 0)))
+        return FATTN_ERR_CUDA;
+      st = fattn_bwd(dev[0], dev[1], dev[2], dev[4], dlse, dev[3], dev[5], dev[6], dev[7], 1, hc, N,
+                     d, scale, causal, ws, L.bwd_ws, p->s_comp);
+      if (st != FATTN_OK) return st;
+      if (!ok(cudaEventRecord(p->bwd_done[s], p->s_comp))) return FATTN_ERR_CUDA;
 
-    // copy out: O and LSE while the backward runs, then the gradients
-    if (!ok(cudaStreamWaitEvent(p->s_out, p->fwd_done[s], 0)) || !copy_out(0) ||
-        !ok(cudaMemcpyAsync(lse + (size_t)h0 * N, dlse, (size_t)hc * N * sizeof(float),
-                            cudaMemcpyDeviceToHost, p->s_out)) ||
-        !ok(cudaStreamWaitEvent(p->s_out, p->bwd_done[s], 0)) || !copy_out(1) || !copy_out(2) ||
-        !copy_out(3) || !ok(cudaEventRecord(p->out_done[s], p->s_out)))
-      return FATTN_ERR_CUDA;
-    h0 += hc;
+      // copy out: O and LSE while the backward runs, then the gradients
+      if (!ok(cudaStreamWaitEvent(p->s_out, p->fwd_done[s], 0)) || !copy_out(0) ||
+          !ok(cudaMemcpyAsync(lse + (size_t)h0 * N, dlse, (size_t)hc * N * sizeof(float),
+                              cudaMemcpyDeviceToHost, p->s_out)) ||
+          !ok(cudaStreamWaitEvent(p->s_out, p->bwd_done[s], 0)) || !copy_out(1) || !copy_out(2) ||
+          !copy_out(3) || !ok(cudaEventRecord(p->out_done[s], p->s_out)))
+        return FATTN_ERR_CUDA;
+      h0 += hc;
+    }
+    n_chunks = c;
+    return FATTN_OK;
+  };
+  st = enqueue_chunks();
+  if (st != FATTN_OK) {
+    // the caller's stream still waits for whatever was enqueued, so that the
+    // host buffers stay in use until those copies have finished
+    for (cudaStream_t q2 : {p->s_in, p->s_comp, p->s_out})
+      if (cudaEventRecord(p->start, q2) == cudaSuccess) cudaStreamWaitEvent(user, p->start, 0);
+    return st;
   }
-  const long long n_chunks = c;
   // the caller's stream continues once the last copy out is done (the copy-out
   // stream runs in order, and each of its chunks waited for that chunk's
   // kernels, which waited for that chunk's copies in)

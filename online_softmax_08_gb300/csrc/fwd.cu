@@ -100,10 +100,11 @@ struct Fwd {
 enum {
   B_Q = 0,
   B_S_FULL = 1,   // [2] MMA -> softmax: S_s ready in TMEM (and every earlier MMA done)
-  B_P_FULL = 3,   // [2] softmax -> MMA: P_s in TMEM and O_s rescaled
+  B_P_FULL = 3,   // [2] softmax -> MMA: P_s in TMEM (both halves)
   B_PV_DONE = 5,  // [2] MMA -> epilogue: O_s += P_s V finished
-  B_MMA_DONE = 7,
-  B_KV_FULL = 8,  // [STAGES], then kv_empty [STAGES]
+  B_P_HALF = 7,   // [2] softmax -> MMA: keys 0-63 of P_s in TMEM and O_s rescaled
+  B_MMA_DONE = 9,
+  B_KV_FULL = 10,  // [STAGES], then kv_empty [STAGES]
 };
 
 // VARLEN: the CTA's sequence comes from p.vl.cu_seqlens (packed head-major
@@ -186,6 +187,7 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_S_FULL + s), 1);
       mbar_init(bar(B_P_FULL + s), 128);
+      mbar_init(bar(B_P_HALF + s), 128);
       mbar_init(bar(B_PV_DONE + s), 1);
     }
     mbar_init(bar(B_MMA_DONE), 1);
@@ -262,14 +264,17 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
         }
         mma_commit_w(bar(B_S_FULL + s));
       };
-      auto issue_pv = [&](int s, int j) {  // O_s += P_s V_j, P_s from TMEM
+      // O_s += P_s V_j over keys [64 half, 64 half + 64), P_s from TMEM
+      auto issue_pv = [&](int s, int j, int half) {
         const uint32_t b = sbase + C::OFF_KV + ((2 * j + 1) % ST) * C::TILE;
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)  // 16 keys = 8 packed TMEM columns per step
+        for (int k = 0; k < C::BN / 32; ++k) {  // 16 keys = 8 packed TMEM columns per step
+          const int kk = half * (C::BN / 32) + k;
           mma_bf16_ts_w(tmem + C::TM_O + s * D, tmem + C::TM_S + s * 128 + kk * 8,
                       sdesc_sw128(b + kk * 16 * 128, C::HALF, 1024), C::IDESC_PV,
                       (j > 0 || kk > 0));
-        mma_commit_w(bar(B_PV_DONE + s));
+        }
+        if (half == 1) mma_commit_w(bar(B_PV_DONE + s));
       };
       // any failed wait means the CTA is aborting: issue nothing more
       bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q), 0, wctx, ERR_SITE_FWD | 0x12));
@@ -288,11 +293,17 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
         for (int s = 0; s < 2; ++s) {
           const int nts = s ? nt1 : nt0;
           if (ok && j < nts) {
+            // the first half of PV runs while the softmax forms the second half of P
             ok = kv_wait(2 * j + 1) &&
-                 __all_sync(0xffffffffu, mbar_wait(bar(B_P_FULL + s), j & 1, wctx, ERR_SITE_FWD | 0x14));
+                 __all_sync(0xffffffffu, mbar_wait(bar(B_P_HALF + s), j & 1, wctx, ERR_SITE_FWD | 0x18));
             if (ok) {
               tc_fence_after();
-              issue_pv(s, j);
+              issue_pv(s, j, 0);
+              ok = __all_sync(0xffffffffu, mbar_wait(bar(B_P_FULL + s), j & 1, wctx, ERR_SITE_FWD | 0x14));
+            }
+            if (ok) {
+              tc_fence_after();
+              issue_pv(s, j, 1);
             }
           }
           if (ok && j + 1 < nts) {  // after the PV above: S_s is overwritten in pipe order
@@ -395,21 +406,27 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
           pk[k / 2 + 1] = pack_bf16x2(p2, p3);
         }
         tmem_st32(tS + h * 32, pk);
+        if (h == 0) {
+          // O_s is rescaled before the first half of PV adds into it (the scores of
+          // the first half are no longer needed, which leaves the registers for it)
+          if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+              tmem_wait_ld(o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(tO + c * 32, o);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(B_P_HALF + s));
+        }
       }
       l_run = l_run * alpha + ((ls0 + ls1) + (ls2 + ls3));
       m_run = m_new;
-
-      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_wait_ld(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + c * 32, o);
-        }
-      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_P_FULL + s));

@@ -26,7 +26,9 @@
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 after it.
 // P_s (bf16, two per 32-bit column) overwrites the first 64 columns of S_s
 // once the softmax has read S_s, and feeds O_s += P_s V as the TMEM A operand,
-// so P never touches shared memory.  The MMA thread issues, per subtile,
+// so P never touches shared memory.  The softmax releases P_s in two halves of
+// 64 keys, and the MMA thread issues the half of O_s += P_s V_j over the first
+// half while the softmax forms the second; per subtile it issues all of
 // O_s += P_s V_j before S_s = Q_s K_{j+1}^T (the pipe runs them in order).
 // Shared memory: Q_0, Q_1 | K/V ring.
 // setmaxnreg regions may not call functions: inline the wait's slow path

@@ -321,10 +321,16 @@ def run_gpu(args):
     assert fattn.fattn_device_error() == 0, "an in-kernel wait timed out"
 
     nan = float("nan")
-    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_ev) if do_fwd else nan
-    pre_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in bwd_ev) if do_bwd else nan
-    main_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in bwd_ev) if do_bwd else nan
-    conv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in bwd_ev) if do_bwd else nan
+    # per-kernel times over the K timed steps: the median is the figure used
+    # (steadier against one slow launch), the mean is reported beside it
+    fwd_t = [a.elapsed_time(b) for a, b in fwd_ev] if do_fwd else [nan]
+    pre_t = [e[0].elapsed_time(e[1]) for e in bwd_ev] if do_bwd else [nan]
+    main_t = [e[1].elapsed_time(e[2]) for e in bwd_ev] if do_bwd else [nan]
+    conv_t = [e[2].elapsed_time(e[3]) for e in bwd_ev] if do_bwd else [nan]
+    fwd_ms, pre_ms, main_ms, conv_ms = (statistics.median(t) for t in (fwd_t, pre_t, main_t, conv_t))
+    means = {name: statistics.mean(t) for name, t in
+             (("fwd_ms", fwd_t), ("preprocess_ms", pre_t), ("main_ms", main_t),
+              ("convert_ms", conv_t))}
     ms_per_step = elapsed_ms / K
     step_flops = (f_fwd if do_fwd else 0.0) + (f_bwd if do_bwd else 0.0)
     value = job_tflops(world, step_flops, ms_per_step)
@@ -421,6 +427,8 @@ def run_gpu(args):
             "bwd": {"ms": pre_ms + main_ms + conv_ms, "preprocess_ms": pre_ms,
                     "main_ms": main_ms, "convert_ms": conv_ms,
                     "tflops": f_bwd / ((pre_ms + main_ms + conv_ms) * 1e-3) / 1e12},
+            "kernel_times": {"statistic": "median over the timed steps (ms); means beside",
+                             "means": means},
             "roofline": roof, "roofline_fwd": roof_fwd, "roofline_fwd_exp": roof_exp,
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": (int(do_fwd) + 3 * int(do_bwd)) * K,
@@ -489,8 +497,8 @@ def run_gpu_varlen(args):
     clk = clocks.stop()
     assert fattn.fattn_device_error() == 0, "an in-kernel wait timed out"
     ms = t0.elapsed_time(t1) / K
-    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
     peak_tf, _, peak_src = peaks()
     fwd_tf, bwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12, f_bwd / (bwd_ms * 1e-3) / 1e12
     line = {

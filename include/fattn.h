@@ -31,8 +31,17 @@
  * launches nothing.  A launch failure returns FATTN_ERR_CUDA.  Faults during
  * execution surface at the caller's next synchronisation, as usual in CUDA.
  * Every wait inside a kernel is bounded; a wait that runs out records a code
- * in a device error word (read with fattn_device_error) and the kernel
- * finishes without hanging.
+ * in a device error word and the kernel finishes without hanging.  The word is
+ * read with fattn_device_error, which returns FATTN_ERR_TIMEOUT while it is
+ * set.  With the environment variable FATTN_DEBUG set to a non-zero value
+ * (read once per process), every entry point that launches work also
+ * synchronises `stream` after enqueueing (not while the stream is being
+ * captured into a graph) and returns FATTN_ERR_TIMEOUT if the word is set.
+ *
+ * The library remembers a few facts per device on first use (kernel
+ * attributes, the SM count and L2 size, the error word's address); the
+ * entries are tied to the device's current context and are set up again after
+ * cudaDeviceReset.
  *
  * The device must be compute capability 10.3 (sm_103a), else
  * FATTN_ERR_UNSUPPORTED.
@@ -67,16 +76,23 @@ int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, 
               int N, int d, float scale, int causal, void* stream);
 
 /* fattn_fwd plus tile instrumentation: when tile_counts (DEVICE pointer to 3
- * unsigned 64-bit counters) is not NULL, the kernel ADDS the number of
- * (128-row query tile, 128-key tile) pairs it processed without masks
- * [0], processed with element masks [1], and skipped as wholly above the
- * causal diagonal [2].  The caller zeroes the counters. */
+ * unsigned 64-bit counters, 8-byte aligned) is not NULL, the kernel ADDS the
+ * number of (128-row query tile, 128-key tile) pairs it processed without
+ * masks [0], processed with element masks [1], and skipped as wholly above
+ * the causal diagonal [2] (page 1, "Causal masking fits inside the tiled
+ * computation": tiles beyond the permitted region are skipped, the ones on
+ * the boundary masked).  The caller zeroes the counters.  The counters are an
+ * argument of the call rather than library state set beforehand, so that
+ * calls from several threads or streams, and calls captured into graphs,
+ * each count into their own buffer. */
 int fattn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int N, int d, float scale, int causal, unsigned long long* tile_counts,
                  void* stream);
 
 /* Bytes of device workspace fattn_bwd needs: an fp32 dQ accumulator
- * [B,H,N,d] and the fp32 row statistic D [B,H,N]. */
+ * [B,H,N,d] and the fp32 row statistic D [B,H,N] (256-byte aligned parts).
+ * No passage of the pages: it sizes the scratch of the backward formulas
+ * below.  Returns 0 for B, H, N < 1 or d not in {64, 128}. */
 size_t fattn_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /* Backward pass.  Inputs q, k, v, o, lse as produced by fattn_fwd and dout
@@ -88,7 +104,11 @@ size_t fattn_bwd_workspace_bytes(int B, int H, int N, int d);
  * recomputation for stored intermediates").
  * workspace: DEVICE memory of at least fattn_bwd_workspace_bytes(B,H,N,d)
  * bytes, 256-byte aligned, owned by the caller; its contents on entry do not
- * matter and are overwritten.  NULL or too small -> FATTN_ERR_WORKSPACE. */
+ * matter and are overwritten.  Too small or misaligned -> FATTN_ERR_WORKSPACE,
+ * nothing launched.  NULL -> the call takes the scratch from the CUDA
+ * stream-ordered allocator: cudaMallocAsync on `stream` before its kernels and
+ * cudaFreeAsync on `stream` after them (workspace_bytes is then ignored); an
+ * allocation failure returns FATTN_ERR_CUDA and launches nothing. */
 int fattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
               const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
               float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
@@ -124,8 +144,10 @@ int fattn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float
                      const int* cu_seqlens, int B, int H, int max_seqlen, int total, int d,
                      float scale, int causal, void* stream);
 
-/* Backward of fattn_fwd_varlen: the layouts above; workspace of at least
- * fattn_bwd_workspace_bytes(1, H, total, d) bytes.  Returns as fattn_bwd. */
+/* Backward of fattn_fwd_varlen ("Backward computation can trade recomputation
+ * for stored intermediates" on page 1, per sequence): the layouts above;
+ * workspace of at least fattn_bwd_workspace_bytes(1, H, total, d) bytes, or
+ * NULL for stream-ordered scratch as in fattn_bwd.  Returns as fattn_bwd. */
 int fattn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const void* dout, void* dq, void* dk, void* dv,
                      const int* cu_seqlens, int B, int H, int max_seqlen, int total, int d,
@@ -154,13 +176,18 @@ int fattn_decode(const void* q, const void* k, const void* v, void* o, float* ls
                  int Nq, int Nkv, int d, float scale, int causal, int n_splits, void* workspace,
                  size_t workspace_bytes, void* stream);
 
-/* Number of key ranges fattn_decode uses for these arguments (0 if invalid). */
+/* Number of key ranges fattn_decode uses for these arguments on the current
+ * device (the automatic count follows its SM count); 0 if invalid.  A sizing
+ * helper of fattn_decode; no passage of its own. */
 int fattn_decode_splits(int B, int H, int Nq, int Nkv, int d, int n_splits);
 
-/* Workspace bytes fattn_decode needs: S x B*H*Nq x (d + 1) fp32 (0 if invalid). */
+/* Workspace bytes fattn_decode needs on the current device: S x B*H*Nq x
+ * (d + 1) fp32 with S = fattn_decode_splits(...); 0 if invalid.  A sizing
+ * helper of fattn_decode; no passage of its own. */
 size_t fattn_decode_workspace_bytes(int B, int H, int Nq, int Nkv, int d, int n_splits);
 
-/* Merge of partial results over disjoint key ranges: o_part [S, rows, d] and
+/* Merge of partial results over disjoint key ranges ("tm_flash_attention_math",
+ * "Proof of exactness": block states combine in any order): o_part [S, rows, d] and
  * lse_part [S, rows] fp32 (range s's normalised output and log-sum-exp; a
  * range in which a row saw no key has lse = -inf) -> lse = log sum_s
  * exp(lse_s), o = sum_s exp(lse_s - lse) o_s as bf16 [rows, d]; a row with
@@ -200,7 +227,8 @@ int fattn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o
                       const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
                       int H, int N, int d, float scale, int causal, void* stream);
 
-/* Bytes of DEVICE workspace fattn_fwd_bwd_host needs: three staging slots,
+/* Sizing helper of fattn_fwd_bwd_host (no passage of its own).
+ * Bytes of DEVICE workspace fattn_fwd_bwd_host needs: three staging slots,
  * each holding Q, K, V, dO, O, dQ, dK, dV and LSE of one chunk of heads plus
  * that chunk's backward workspace.  heads_per_chunk = 0 selects the library's
  * chunk size for the current device (the same one fattn_fwd_bwd_host picks
@@ -230,34 +258,23 @@ int fattn_fwd_bwd_host(const void* q, const void* k, const void* v, const void* 
                        size_t workspace_bytes, void* stream);
 
 /* Tile shape used by a pass (0 = forward, 1 = backward) for head size d:
- * rows of Q per tile and keys per K/V tile.  Returns FATTN_OK or
- * FATTN_ERR_UNSUPPORTED. */
+ * rows of Q per tile and keys per K/V tile; 128 x 128, the tile of "Decoding
+ * flash attention" ("The idea: never build the matrix").  block_q and block_k may be NULL.
+ * Returns FATTN_OK, FATTN_ERR_UNSUPPORTED (d) or FATTN_ERR_INVALID_ARG (pass). */
 int fattn_tile_sizes(int d, int pass, int* block_q, int* block_k);
 
 /* Read (and, if clear != 0, reset) the device error word of the current
- * device: 0 if no in-kernel wait ran out since the last reset, else the code
- * of the first one.  Synchronises the device.  Returns FATTN_OK or
- * FATTN_ERR_CUDA. */
+ * device: *code = 0 if no in-kernel wait ran out since the last reset, else
+ * the code of the first one (low byte: the waiting role; next byte: the
+ * kernel).  Synchronises the device.  Returns FATTN_OK when the word was 0,
+ * FATTN_ERR_TIMEOUT when it was set (with *code written, and cleared if
+ * asked), FATTN_ERR_INVALID_ARG for a NULL code, FATTN_ERR_CUDA.  The pages
+ * have no counterpart: it reports this library's bounded waits. */
 int fattn_device_error(unsigned int* code, int clear);
 
-/* Failure-path check: launches one warp that waits, through the kernels'
- * bounded-wait routine, on a barrier that nothing completes, with a short
- * limit (2^21 SM clock cycles, about 1 ms).  The wait then records code 0x301
- * in the device error word (read it with fattn_device_error) and the kernel
- * returns; the context stays usable.  Asynchronous on stream.  Returns
- * FATTN_OK, FATTN_ERR_UNSUPPORTED or FATTN_ERR_CUDA.  The pages have no
- * counterpart; it tests this library's own timeout reporting. */
-int fattn_check_wait_timeout(void* stream);
-
-/* Measured throughput of the exponential unit of the current device, in ex2
- * evaluations per second: a kernel of independent ex2.approx chains on every
- * SM, timed with events on `stream` (a warm-up launch, then one timed launch;
- * the call synchronises with the timed launch).  It is the second ceiling of
- * the forward pass, which takes one exponential per visible score.  Returns
- * FATTN_OK, FATTN_ERR_INVALID_ARG (per_second NULL) or FATTN_ERR_CUDA. */
-int fattn_ex2_throughput(double* per_second, void* stream);
-
-/* Human-readable name of a status code (static storage). */
+/* Human-readable name of a status code (static storage).  No passage: a helper.
+ * The library also exports two test and measurement hooks, declared apart in
+ * fattn_testing.h; they are not part of this interface. */
 const char* fattn_status_string(int status);
 
 #ifdef __cplusplus

@@ -1,6 +1,7 @@
 // api.cu -- the C-ABI of libfattn: argument checks, TMA descriptors, launches.
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <cudaTypedefs.h>
@@ -20,10 +21,11 @@ __device__ unsigned int g_error_word;  // first in-kernel wait that ran out (0 =
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
-  bool probed = false;
+  unsigned long long ctx = 0;   // context the entry was filled in (0: not yet)
   bool supported = false;
   unsigned int* err = nullptr;  // device address of g_error_word
   int n_sm = 0;                 // streaming multiprocessors
+  long long l2_bytes = 0;       // L2 cache size
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -35,14 +37,18 @@ int current_device(DeviceInfo** out) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FATTN_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceInfo& info = g_dev[dev];
-  if (!info.probed) {
-    int major = 0, minor = 0;
+  const unsigned long long ctx = current_context_id();
+  if (ctx == 0 || info.ctx != ctx) {
+    int major = 0, minor = 0, l2 = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return FATTN_ERR_CUDA;
     info.supported = (major == 10 && minor == 3);
-    if (cudaDeviceGetAttribute(&info.n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    if (cudaDeviceGetAttribute(&info.n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
       return FATTN_ERR_CUDA;
+    info.l2_bytes = l2;
+    // the symbol lookup also makes the device's primary context current
     void* addr = nullptr;
     if (cudaGetSymbolAddress(&addr, g_error_word) != cudaSuccess) return FATTN_ERR_CUDA;
     info.err = static_cast<unsigned int*>(addr);
@@ -55,7 +61,7 @@ int current_device(DeviceInfo** out) {
         return FATTN_ERR_CUDA;
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
-    info.probed = true;
+    info.ctx = current_context_id();
   }
   if (!info.supported) return FATTN_ERR_UNSUPPORTED;
   *out = &info;
@@ -93,10 +99,75 @@ int check_common(int B, int H, int N, int d, float scale) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Share of the 129 MB L2 that the CTAs in flight of the dense kernels may read from.
-constexpr long long kL2GroupBytes = 32LL << 20;
+// Heads per group of the dense grid order: as many as fit their tensors
+// (bytes_per_head) in a quarter of L2, the share measured best for both
+// kernels (an eighth and a half were slower), at least one.
+int l2_group(const DeviceInfo& dev, long long bytes_per_head) {
+  return (int)std::max<long long>(1, (dev.l2_bytes / 4) / bytes_per_head);
+}
 
 }  // namespace
+
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static const GetCurrent get_current = [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    return cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+                       cudaSuccess &&
+                   q == cudaDriverEntryPointSuccess
+               ? reinterpret_cast<GetCurrent>(fn)
+               : nullptr;
+  }();
+  static const GetId get_id = [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    return cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+                       cudaSuccess &&
+                   q == cudaDriverEntryPointSuccess
+               ? reinterpret_cast<GetId>(fn)
+               : nullptr;
+  }();
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c ||
+      get_id(c, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+int device_sm_count() {
+  DeviceInfo* dev = nullptr;
+  return current_device(&dev) == FATTN_OK ? dev->n_sm : 0;
+}
+
+long long device_l2_bytes() {
+  DeviceInfo* dev = nullptr;
+  return current_device(&dev) == FATTN_OK ? dev->l2_bytes : 0;
+}
+
+namespace {
+bool debug_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("FATTN_DEBUG");
+    return v && *v && strcmp(v, "0") != 0;
+  }();
+  return on;
+}
+}  // namespace
+
+int debug_post_call(int status, cudaStream_t stream) {
+  if (status != FATTN_OK || !debug_enabled()) return status;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return FATTN_ERR_CUDA;
+  if (cs != cudaStreamCaptureStatusNone) return status;  // nothing has run yet
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FATTN_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word)) != cudaSuccess) return FATTN_ERR_CUDA;
+  return word ? FATTN_ERR_TIMEOUT : FATTN_OK;
+}
+
 }  // namespace fattn
 
 using namespace fattn;
@@ -139,8 +210,8 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
   p.err = dev->err;
   p.vl = g.vl;
   p.o = static_cast<uint16_t*>(o);
-  // dense: groups of heads whose K and V (4 N d bytes a head) fit in 32 MiB of L2
-  p.group = (int)std::max<long long>(1, (kL2GroupBytes) / (4LL * g.N * d));
+  // dense: groups of heads whose K and V (4 N d bytes a head) fit in a quarter of L2
+  p.group = l2_group(*dev, 4LL * g.N * d);
   cudaError_t e = launch_fwd(d, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
@@ -149,24 +220,15 @@ size_t workspace_bytes_for_rows(long long rows, int d) {
   return align256((size_t)rows * d * sizeof(float)) + align256((size_t)rows * sizeof(float));
 }
 
-int run_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-            const void* dout, void* dq, void* dk, void* dv, int d, float scale, int causal,
-            const Geometry& g, void* workspace, size_t workspace_bytes,
-            void* const* phase_events, void* stream) {
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-    return FATTN_ERR_INVALID_ARG;
+// The kernels of one backward call on a workspace that is already in place.
+int launch_bwd_all(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dout, void* dq, void* dk, void* dv, int d, float scale, int causal,
+                   const Geometry& g, const DeviceInfo& dev, void* workspace,
+                   void* const* phase_events, cudaStream_t s) {
   const long long rows = g.map_rows * g.map_z;
-  const size_t need = workspace_bytes_for_rows(rows, d);
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
-    return FATTN_ERR_WORKSPACE;
-  DeviceInfo* dev = nullptr;
-  const int st = current_device(&dev);
-  if (st != FATTN_OK) return st;
   float* dq_acc = static_cast<float*>(workspace);
   float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                           align256((size_t)rows * d * sizeof(float)));
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   int bq = 0, bk = 0;
   fattn_tile_sizes(d, 1, &bq, &bk);
   const long long R = g.map_rows, Z = g.map_z;
@@ -184,7 +246,7 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const fl
            cudaEventRecord(static_cast<cudaEvent_t>(phase_events[i]), s) == cudaSuccess;
   };
   if (!mark(0)) return FATTN_ERR_CUDA;
-  if (launch_bwd_preprocess(o, dout, delta, dq_acc, rows, d, s) != cudaSuccess)
+  if (launch_bwd_preprocess(o, dout, delta, dq_acc, rows, d, dev.n_sm, s) != cudaSuccess)
     return FATTN_ERR_CUDA;
   if (!mark(1)) return FATTN_ERR_CUDA;
   BwdParams p{};
@@ -196,20 +258,53 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const fl
   p.lse = lse;
   p.delta = delta;
   p.dq_acc = dq_acc;
-  p.err = dev->err;
+  p.err = dev.err;
   p.vl = g.vl;
   p.dk = static_cast<uint16_t*>(dk);
   p.dv = static_cast<uint16_t*>(dv);
   // dense: groups of heads whose Q, dO (bf16) and dQ accumulator (fp32), 8 N d
-  // bytes a head, fit in 32 MiB of L2
-  p.group = (int)std::max<long long>(1, (kL2GroupBytes) / (8LL * g.N * d));
+  // bytes a head, fit in a quarter of L2
+  p.group = l2_group(dev, 8LL * g.N * d);
   cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, tdk, tdv, tdq, p, s);
   if (e == cudaErrorNotSupported) return FATTN_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return FATTN_ERR_CUDA;
   if (!mark(2)) return FATTN_ERR_CUDA;
-  if (launch_bwd_convert(dq_acc, dq, rows * d, scale, s) != cudaSuccess) return FATTN_ERR_CUDA;
+  if (launch_bwd_convert(dq_acc, dq, rows * d, scale, dev.n_sm, s) != cudaSuccess)
+    return FATTN_ERR_CUDA;
   if (!mark(3)) return FATTN_ERR_CUDA;
   return FATTN_OK;
+}
+
+int run_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+            const void* dout, void* dq, void* dk, void* dv, int d, float scale, int causal,
+            const Geometry& g, void* workspace, size_t workspace_bytes,
+            void* const* phase_events, void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FATTN_ERR_INVALID_ARG;
+  const long long rows = g.map_rows * g.map_z;
+  const size_t need = workspace_bytes_for_rows(rows, d);
+  if (workspace && ((reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need))
+    return FATTN_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  const int st = current_device(&dev);
+  if (st != FATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (workspace)
+    return launch_bwd_all(q, k, v, o, lse, dout, dq, dk, dv, d, scale, causal, g, *dev, workspace,
+                          phase_events, s);
+  // no workspace from the caller: stream-ordered scratch, allocated and freed
+  // on `stream` around the kernels (256 spare bytes keep the 256-byte alignment)
+  void* raw = nullptr;
+  if (cudaMallocAsync(&raw, need + 256, s) != cudaSuccess) {
+    cudaGetLastError();  // an allocation failure is not sticky: clear it
+    return FATTN_ERR_CUDA;
+  }
+  void* ws = reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(raw) + 255u) & ~(uintptr_t)255u);
+  const int r = launch_bwd_all(q, k, v, o, lse, dout, dq, dk, dv, d, scale, causal, g, *dev, ws,
+                               phase_events, s);
+  if (cudaFreeAsync(raw, s) != cudaSuccess) return FATTN_ERR_CUDA;
+  return r;
 }
 
 Geometry dense_geometry(int B, int H, int N) {
@@ -235,7 +330,9 @@ extern "C" int fattn_fwd_ex(const void* q, const void* k, const void* v, void* o
                             unsigned long long* tile_counts, void* stream) {
   const int st = check_common(B, H, N, d, scale);
   if (st != FATTN_OK) return st;
-  return run_fwd(q, k, v, o, lse, d, scale, causal, dense_geometry(B, H, N), tile_counts, stream);
+  return debug_post_call(
+      run_fwd(q, k, v, o, lse, d, scale, causal, dense_geometry(B, H, N), tile_counts, stream),
+      static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -250,7 +347,8 @@ extern "C" int fattn_fwd_varlen(const void* q, const void* k, const void* v, voi
   if (st != FATTN_OK) return st;
   if (total == 0 || max_seqlen == 0) return FATTN_OK;  // no rows: nothing to compute
   const Geometry g{total, H, H, max_seqlen, Varlen{cu_seqlens, B, H, total}};
-  return run_fwd(q, k, v, o, lse, d, scale, causal, g, nullptr, stream);
+  return debug_post_call(run_fwd(q, k, v, o, lse, d, scale, causal, g, nullptr, stream),
+                         static_cast<cudaStream_t>(stream));
 }
 
 namespace fattn {
@@ -258,21 +356,21 @@ namespace {
 
 // Key ranges of a split call: n_tiles 128-key tiles cut into ranges of
 // tiles_per_split tiles.  n_splits = 0 picks enough ranges for about ten
-// waves of CTAs over the 152 SMs (measured best at B4 H32 Nq1 Nkv32768: 94 %
-// of the copy bandwidth, against 90 % for one wave), keeping at least four
-// tiles per range; a request is capped at one range per tile and empty ranges
-// are dropped.
+// waves of CTAs over the device's n_sm SMs (measured best at B4 H32 Nq1
+// Nkv32768: 94 % of the copy bandwidth, against 90 % for one wave), keeping at
+// least four tiles per range; a request is capped at one range per tile and
+// empty ranges are dropped.
 struct SplitPlan {
   int n_splits;
   int tiles_per_split;
 };
-SplitPlan plan_splits(long long units, int Nq, int Nkv, int n_splits) {
+SplitPlan plan_splits(long long units, int Nq, int Nkv, int n_splits, int n_sm) {
   const int n_tiles = (Nkv + 127) / 128;
   const long long n_qb = (Nq + 255) / 256;
   long long want = n_splits;
   if (want <= 0) {
     const long long ctas = units * n_qb;
-    want = (10 * 152 + ctas - 1) / ctas;
+    want = (10LL * n_sm + ctas - 1) / ctas;
     if (want > n_tiles / 4) want = n_tiles / 4;
   }
   if (want > n_tiles) want = n_tiles;
@@ -298,13 +396,17 @@ size_t decode_ws_bytes(long long rows, int d, int S) {
 
 extern "C" int fattn_decode_splits(int B, int H, int Nq, int Nkv, int d, int n_splits) {
   if (check_decode(B, H, Nq, Nkv, d, 1.f, n_splits) != FATTN_OK) return 0;
-  return plan_splits((long long)B * H, Nq, Nkv, n_splits).n_splits;
+  DeviceInfo* dev = nullptr;
+  if (current_device(&dev) != FATTN_OK) return 0;
+  return plan_splits((long long)B * H, Nq, Nkv, n_splits, dev->n_sm).n_splits;
 }
 
 extern "C" size_t fattn_decode_workspace_bytes(int B, int H, int Nq, int Nkv, int d,
                                                int n_splits) {
   if (check_decode(B, H, Nq, Nkv, d, 1.f, n_splits) != FATTN_OK) return 0;
-  const SplitPlan sp = plan_splits((long long)B * H, Nq, Nkv, n_splits);
+  DeviceInfo* dev = nullptr;
+  if (current_device(&dev) != FATTN_OK) return 0;
+  const SplitPlan sp = plan_splits((long long)B * H, Nq, Nkv, n_splits, dev->n_sm);
   return decode_ws_bytes((long long)B * H * Nq, d, sp.n_splits);
 }
 
@@ -316,13 +418,12 @@ extern "C" int fattn_decode(const void* q, const void* k, const void* v, void* o
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FATTN_ERR_INVALID_ARG;
   const long long BH = (long long)B * H, rows = BH * Nq;
-  const SplitPlan sp = plan_splits(BH, Nq, Nkv, n_splits);
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
-      workspace_bytes < decode_ws_bytes(rows, d, sp.n_splits))
-    return FATTN_ERR_WORKSPACE;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FATTN_ERR_WORKSPACE;
   DeviceInfo* dev = nullptr;
   st = current_device(&dev);
   if (st != FATTN_OK) return st;
+  const SplitPlan sp = plan_splits(BH, Nq, Nkv, n_splits, dev->n_sm);
+  if (workspace_bytes < decode_ws_bytes(rows, d, sp.n_splits)) return FATTN_ERR_WORKSPACE;
   CUtensorMap tq, tk, tv;
   if (!make_bf16_map(&tq, q, d, Nq, BH, 128) || !make_bf16_map(&tk, k, d, Nkv, BH, 128) ||
       !make_bf16_map(&tv, v, d, Nkv, BH, 128))
@@ -345,7 +446,7 @@ extern "C" int fattn_decode(const void* q, const void* k, const void* v, void* o
   if (launch_fwd_split(d, tq, tk, tv, tq, p, s) != cudaSuccess) return FATTN_ERR_CUDA;
   if (launch_merge(o_part, lse_part, sp.n_splits, rows, d, o, lse, s) != cudaSuccess)
     return FATTN_ERR_CUDA;
-  return FATTN_OK;
+  return debug_post_call(FATTN_OK, s);
 }
 
 extern "C" int fattn_merge_partials(const float* o_part, const float* lse_part, int n_splits,
@@ -357,10 +458,11 @@ extern "C" int fattn_merge_partials(const float* o_part, const float* lse_part, 
   DeviceInfo* dev = nullptr;
   const int st = current_device(&dev);
   if (st != FATTN_OK) return st;
-  return launch_merge(o_part, lse_part, n_splits, rows, d, o, lse, static_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
-             ? FATTN_OK
-             : FATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return debug_post_call(
+      launch_merge(o_part, lse_part, n_splits, rows, d, o, lse, s) == cudaSuccess ? FATTN_OK
+                                                                                  : FATTN_ERR_CUDA,
+      s);
 }
 
 extern "C" int fattn_softmax_rows(const float* x, float* y, float* lse, long long rows, int cols,
@@ -371,10 +473,11 @@ extern "C" int fattn_softmax_rows(const float* x, float* y, float* lse, long lon
   DeviceInfo* dev = nullptr;
   const int st = current_device(&dev);
   if (st != FATTN_OK) return st;
-  return launch_softmax_rows(x, y, lse, rows, cols, dev->n_sm, static_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
-             ? FATTN_OK
-             : FATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return debug_post_call(
+      launch_softmax_rows(x, y, lse, rows, cols, dev->n_sm, s) == cudaSuccess ? FATTN_OK
+                                                                              : FATTN_ERR_CUDA,
+      s);
 }
 
 extern "C" size_t fattn_bwd_workspace_bytes(int B, int H, int N, int d) {
@@ -388,8 +491,10 @@ extern "C" int fattn_bwd_ex(const void* q, const void* k, const void* v, const v
                             size_t workspace_bytes, void* const* phase_events, void* stream) {
   const int st = check_common(B, H, N, d, scale);
   if (st != FATTN_OK) return st;
-  return run_bwd(q, k, v, o, lse, dout, dq, dk, dv, d, scale, causal, dense_geometry(B, H, N),
-                 workspace, workspace_bytes, phase_events, stream);
+  return debug_post_call(run_bwd(q, k, v, o, lse, dout, dq, dk, dv, d, scale, causal,
+                                 dense_geometry(B, H, N), workspace, workspace_bytes, phase_events,
+                                 stream),
+                         static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fattn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
@@ -401,8 +506,9 @@ extern "C" int fattn_bwd_varlen(const void* q, const void* k, const void* v, con
   if (st != FATTN_OK) return st;
   if (total == 0 || max_seqlen == 0) return FATTN_OK;  // no rows: nothing to compute
   const Geometry g{total, H, H, max_seqlen, Varlen{cu_seqlens, B, H, total}};
-  return run_bwd(q, k, v, o, lse, dout, dq, dk, dv, d, scale, causal, g, workspace,
-                 workspace_bytes, nullptr, stream);
+  return debug_post_call(run_bwd(q, k, v, o, lse, dout, dq, dk, dv, d, scale, causal, g, workspace,
+                                 workspace_bytes, nullptr, stream),
+                         static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fattn_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -448,8 +554,9 @@ extern "C" int fattn_check_wait_timeout(void* stream) {
   DeviceInfo* dev = nullptr;
   const int st = current_device(&dev);
   if (st != FATTN_OK) return st;
-  fattn::wait_timeout_check_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev->err);
-  return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  fattn::wait_timeout_check_kernel<<<1, 32, 0, s>>>(dev->err);
+  return debug_post_call(cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA, s);
 }
 
 extern "C" int fattn_device_error(unsigned int* code, int clear) {
@@ -463,7 +570,7 @@ extern "C" int fattn_device_error(unsigned int* code, int clear) {
     if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess)
       return FATTN_ERR_CUDA;
   }
-  return FATTN_OK;
+  return v ? FATTN_ERR_TIMEOUT : FATTN_OK;
 }
 
 extern "C" const char* fattn_status_string(int status) {

@@ -644,7 +644,7 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   using C = Bwd<D>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
   static_assert(C::TM_Y + 128 <= 512, "TMEM budget");
-  static int prepared[64];
+  static unsigned long long prepared[64];
   cudaError_t e = prepare_once(prepared, [] {
     cudaError_t r = cudaFuncSetAttribute(fattn_bwd_kernel<D, VARLEN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);

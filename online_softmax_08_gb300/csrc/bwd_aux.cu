@@ -75,21 +75,18 @@ __global__ void __launch_bounds__(256) convert_kernel(const float4* __restrict__
   }
 }
 
-unsigned grid_for(long long work, int threads) {
-  int dev = 0, sms = 152;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+unsigned grid_for(long long work, int threads, int n_sm) {
   const long long want = (work + threads - 1) / threads;
-  const long long cap = (long long)sms * 8;  // 8 resident 256-thread blocks per SM
+  const long long cap = (long long)n_sm * 8;  // 8 resident 256-thread blocks per SM
   return (unsigned)(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* delta, float* dq_acc,
-                                  long long rows, int d, cudaStream_t stream) {
+                                  long long rows, int d, int n_sm, cudaStream_t stream) {
   const long long work = rows * (d / 8);
-  const unsigned grid = grid_for(work, 256);
+  const unsigned grid = grid_for(work, 256, n_sm);
   if (d == 128)
     preprocess_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(o),
                                                      static_cast<const uint4*>(dout), delta,
@@ -104,9 +101,9 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* delta,
 }
 
 cudaError_t launch_bwd_convert(const float* dq_acc, void* dq, long long n, float scale,
-                               cudaStream_t stream) {
+                               int n_sm, cudaStream_t stream) {
   const long long n8 = n / 8;
-  convert_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
+  convert_kernel<<<grid_for(n8, 256, n_sm), 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
                                                         static_cast<uint4*>(dq), n8, scale);
   return cudaGetLastError();
 }

@@ -108,18 +108,37 @@ __device__ __forceinline__ bool seq_view(const Varlen& vl, int dense_N, int seq,
   return true;
 }
 
+// Identity of the calling thread's current CUDA context (the device's primary
+// context under the runtime API): a process-unique id, 0 when no context is
+// current yet.  Per-device caches remember the context they were filled in and
+// fill themselves again when it changes, since cudaDeviceReset destroys the
+// primary context and every attribute, address, stream and event made in it.
+unsigned long long current_context_id();
+
 // Per-device one-time preparation of a kernel (its shared-memory opt-in and
 // register checks), so that later calls, including calls under stream capture
-// into a CUDA graph, make no attribute calls.  flags: one int per device.
+// into a CUDA graph, make no attribute calls.  ctx_ids: one entry per device,
+// the context the preparation was made in (0: not prepared).
 template <typename Prep>
-cudaError_t prepare_once(int (&flags)[64], Prep prep) {
+cudaError_t prepare_once(unsigned long long (&ctx_ids)[64], Prep prep) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (__atomic_load_n(&flags[dev], __ATOMIC_ACQUIRE)) return cudaSuccess;
+  const unsigned long long ctx = current_context_id();
+  if (ctx != 0 && __atomic_load_n(&ctx_ids[dev], __ATOMIC_ACQUIRE) == ctx) return cudaSuccess;
   const cudaError_t e = prep();  // idempotent: two threads may both run it
-  if (e == cudaSuccess) __atomic_store_n(&flags[dev], 1, __ATOMIC_RELEASE);
+  if (e == cudaSuccess) __atomic_store_n(&ctx_ids[dev], current_context_id(), __ATOMIC_RELEASE);
   return e;
 }
+
+// Device facts the launchers size their grids and groups with.
+int device_sm_count();             // streaming multiprocessors of the current device (0: error)
+long long device_l2_bytes();       // L2 cache of the current device (0: error)
+
+// When the environment variable FATTN_DEBUG is set to a non-zero value, an
+// entry point that enqueued work successfully synchronises `stream` (unless it
+// is being captured into a graph) and returns FATTN_ERR_TIMEOUT if the device
+// error word is set; otherwise it returns `status` unchanged.
+int debug_post_call(int status, cudaStream_t stream);
 
 // Launchers (one per translation unit).  Return cudaSuccess or the launch error.
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -135,12 +154,12 @@ cudaError_t launch_merge(const float* o_part, const float* lse_part, int n_split
                          int d, void* o, float* lse, cudaStream_t stream);
 
 cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* delta, float* dq_acc,
-                                  long long rows, int d, cudaStream_t stream);
+                                  long long rows, int d, int n_sm, cudaStream_t stream);
 cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
                             const CUtensorMap& tdk, const CUtensorMap& tdv,
                             const CUtensorMap& tdq_acc, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_convert(const float* dq_acc, void* dq, long long n, float scale,
-                               cudaStream_t stream);
+                               int n_sm, cudaStream_t stream);
 
 }  // namespace fattn

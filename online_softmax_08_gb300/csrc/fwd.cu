@@ -537,7 +537,7 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   using C = Fwd<D>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
   static_assert(!(VARLEN && SPLIT), "split-KV is dense only");
-  static int prepared[64];
+  static unsigned long long prepared[64];
   cudaError_t e = prepare_once(prepared, [] {
     cudaError_t r = cudaFuncSetAttribute(fattn_fwd_kernel<D, VARLEN, SPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);

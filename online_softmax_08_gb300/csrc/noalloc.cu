@@ -22,33 +22,45 @@
 //     on every call;
 //   * the first call on each device looks up the array's device address
 //     (cudaGetSymbolAddress, with that device current) and caches it, so that
-//     first call should come before any stream capture.
+//     first call should come before any stream capture.  The cache remembers
+//     the context it was filled in: after cudaDeviceReset the next call looks
+//     the address up again.
+#include <math.h>
 #include <stdint.h>
 
 #include <mutex>
 
 #include "../../include/fattn.h"
+#include "common.cuh"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FATTN_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices];
+struct ScratchAddress {
+  unsigned long long ctx = 0;  // context the address was looked up in (0: not yet)
+  void* ptr = nullptr;
+};
+ScratchAddress g_scratch[kMaxDevices];
 std::mutex g_scratch_mu;
 
-// Device address of the scratch array on the current device (set up once per device).
+// Device address of the scratch array on the current device (set up once per
+// device and context).
 int scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FATTN_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  ScratchAddress& e = g_scratch[dev];
+  const unsigned long long ctx = fattn::current_context_id();
+  if (ctx == 0 || e.ctx != ctx) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress((void**)&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
       return FATTN_ERR_CUDA;
-    g_scratch_ptr[dev] = ptr;
+    e.ptr = ptr;
+    e.ctx = fattn::current_context_id();  // the lookup made the context current
   }
-  *out = g_scratch_ptr[dev];
+  *out = e.ptr;
   return FATTN_OK;
 }
 
@@ -58,9 +70,14 @@ extern "C" int fattn_bwd_noalloc(const void* q, const void* k, const void* v, co
                                  const float* lse, const void* dout, void* dq, void* dk,
                                  void* dv, int B, int H, int N, int d, float scale, int causal,
                                  void* stream) {
-  const size_t need = fattn_bwd_workspace_bytes(B, H, N, d);
-  if (need == 0) return (d != 64 && d != 128) ? FATTN_ERR_UNSUPPORTED : FATTN_ERR_INVALID_ARG;
-  if (need > (size_t)FATTN_NOALLOC_SCRATCH_BYTES) return FATTN_ERR_WORKSPACE;
+  // fattn_bwd's size checks, in its order, before the scratch-size check, so
+  // that both entry points give the same status for the same bad arguments
+  if (B < 1 || H < 1 || N < 1) return FATTN_ERR_INVALID_ARG;
+  if ((long long)B * H * N >= (1LL << 31)) return FATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  if (fattn_bwd_workspace_bytes(B, H, N, d) > (size_t)FATTN_NOALLOC_SCRATCH_BYTES)
+    return FATTN_ERR_WORKSPACE;
   void* scratch = nullptr;
   const int st = scratch_for_current_device(&scratch);
   if (st != FATTN_OK) return st;

@@ -234,7 +234,7 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* lse, long long 
   if (rows <= 0 || cols <= 0) return cudaSuccess;
   const int staged = cols <= kSmemCols ? 1 : 0;
   const size_t smem = staged ? (size_t)((cols + 3) & ~3) * sizeof(float) : 0;
-  static int prepared[64];
+  static unsigned long long prepared[64];
   cudaError_t e = prepare_once(prepared, [] {
     return cudaFuncSetAttribute(softmax_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)(kSmemCols * sizeof(float)));

@@ -25,6 +25,7 @@
 #include <mutex>
 
 #include "../../include/fattn.h"
+#include "common.cuh"
 
 namespace {
 
@@ -32,7 +33,7 @@ constexpr int kSlots = 3;
 constexpr int kMaxDevices = 64;
 
 struct Pipeline {
-  bool ready = false;
+  unsigned long long ctx = 0;  // context the streams and events were made in (0: none yet)
   int n_sm = 0;
   cudaStream_t s_in = nullptr, s_comp = nullptr, s_out = nullptr;
   cudaEvent_t start = nullptr;
@@ -48,7 +49,9 @@ int pipeline_for_current_device(Pipeline** out) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FATTN_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_pipe_mu);
   Pipeline& p = g_pipe[dev];
-  if (!p.ready) {
+  const unsigned long long ctx = fattn::current_context_id();
+  if (ctx == 0 || p.ctx != ctx) {
+    // first use, or the context was reset: the old handles died with it
     const unsigned sf = cudaStreamNonBlocking;
     const unsigned ef = cudaEventDisableTiming;
     if (cudaDeviceGetAttribute(&p.n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -61,7 +64,7 @@ int pipeline_for_current_device(Pipeline** out) {
       for (cudaEvent_t* e : {&p.qkv_in[i], &p.do_in[i], &p.fwd_done[i], &p.bwd_done[i],
                              &p.out_done[i]})
         if (cudaEventCreateWithFlags(e, ef) != cudaSuccess) return FATTN_ERR_CUDA;
-    p.ready = true;
+    p.ctx = fattn::current_context_id();
   }
   *out = &p;
   return FATTN_OK;
@@ -231,5 +234,5 @@ extern "C" int fattn_fwd_bwd_host(const void* q, const void* k, const void* v, c
   // kernels, which waited for that chunk's copies in)
   const int last = (int)((n_chunks - 1) % kSlots);
   if (!ok(cudaStreamWaitEvent(user, p->out_done[last], 0))) return FATTN_ERR_CUDA;
-  return FATTN_OK;
+  return fattn::debug_post_call(FATTN_OK, user);
 }

@@ -36,7 +36,6 @@ SIGNATURES = {
                                _i, _vp]),
     "fattn_tile_sizes": (_i, [_i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "fattn_device_error": (_i, [ctypes.POINTER(ctypes.c_uint), _i]),
-    "fattn_check_wait_timeout": (_i, [_vp]),
     "fattn_softmax_rows": (_i, [_vp, _vp, _vp, ctypes.c_longlong, _i, _vp]),
     "fattn_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz, _vp]),
     "fattn_decode_splits": (_i, [_i, _i, _i, _i, _i, _i]),
@@ -48,8 +47,14 @@ SIGNATURES = {
     "fattn_fwd_bwd_host_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "fattn_fwd_bwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f,
                                 _i, _i, _vp, _sz, _vp]),
-    "fattn_ex2_throughput": (_i, [ctypes.POINTER(ctypes.c_double), _vp]),
     "fattn_status_string": (ctypes.c_char_p, [_i]),
+}
+
+# The test and measurement hooks of include/fattn_testing.h (exported by the
+# same library, not part of the attention interface).
+TESTING_SIGNATURES = {
+    "fattn_check_wait_timeout": (_i, [_vp]),
+    "fattn_ex2_throughput": (_i, [ctypes.POINTER(ctypes.c_double), _vp]),
 }
 
 _lock = threading.Lock()
@@ -73,7 +78,7 @@ def load(path=None):
             raise RuntimeError("libfattn.so not found at %s: build it with "
                                "`python -c 'import __graft_entry__ as g; g.build()'`" % p)
         lib = ctypes.CDLL(p)
-        for name, (res, args) in SIGNATURES.items():
+        for name, (res, args) in list(SIGNATURES.items()) + list(TESTING_SIGNATURES.items()):
             fn = getattr(lib, name)
             fn.restype = res
             fn.argtypes = args
@@ -185,9 +190,16 @@ def fattn_tile_sizes(d, pass_):
     return bq.value, bk.value
 
 
+FATTN_ERR_TIMEOUT = 5
+
+
 def fattn_device_error(clear=True):
+    """The device error word (0: no in-kernel wait ran out); the C call returns
+    FATTN_ERR_TIMEOUT while the word is set, which is a successful read here."""
     code = ctypes.c_uint(0)
-    _check("fattn_device_error", load().fattn_device_error(ctypes.byref(code), int(bool(clear))))
+    st = load().fattn_device_error(ctypes.byref(code), int(bool(clear)))
+    if st not in (FATTN_OK, FATTN_ERR_TIMEOUT):
+        raise FattnError("fattn_device_error", st)
     return code.value
 
 
@@ -232,9 +244,16 @@ def forward(q, k, v, scale, causal, tile_counts=None, stream=None):
 
 
 def backward(q, k, v, o, lse, do, scale, causal, workspace=None, stream=None):
-    """dQ, dK, dV for dL/dO = do."""
+    """dQ, dK, dV for dL/dO = do.  workspace: None (a torch allocation), a
+    device tensor, or "stream" (the library's stream-ordered scratch: the C
+    call gets a NULL workspace)."""
     B, H, N, d = _shape(q)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if isinstance(workspace, str):
+        if workspace != "stream":
+            raise ValueError(workspace)
+        fattn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, None, 0, stream)
+        return dq, dk, dv
     nbytes = fattn_bwd_workspace_bytes(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)

@@ -1,6 +1,7 @@
 """The C-ABI libraries load and export every entry point their headers declare
-(include/fattn.h: libfattn; include/fattn_host.h: libfattn_host); argument
-checks that fail before any device work run on the CPU."""
+(include/fattn.h and the test hooks of include/fattn_testing.h: libfattn;
+include/fattn_host.h: libfattn_host); argument checks that fail before any
+device work run on the CPU."""
 import os
 import re
 
@@ -26,7 +27,7 @@ def _declared(header):
 
 def test_headers_are_the_two_libraries():
     assert sorted(f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")) == \
-        ["fattn.h", "fattn_host.h"]
+        ["fattn.h", "fattn_host.h", "fattn_testing.h"]
 
 
 def test_every_declared_symbol_is_exported_and_bound(lib):
@@ -36,6 +37,15 @@ def test_every_declared_symbol_is_exported_and_bound(lib):
         assert hasattr(lib, name), name
         assert name in fattn.SIGNATURES, name
     assert set(fattn.SIGNATURES) == declared
+
+
+def test_test_hooks_are_declared_apart(lib):
+    hooks = _declared("fattn_testing.h")
+    assert hooks == {"fattn_check_wait_timeout", "fattn_ex2_throughput"}
+    assert not hooks & _declared("fattn.h")
+    for name in hooks:
+        assert hasattr(lib, name), name
+    assert set(fattn.TESTING_SIGNATURES) == hooks
 
 
 def test_every_host_symbol_is_exported_and_bound(lib):
@@ -78,7 +88,6 @@ def test_argument_checks_before_any_device_call(lib):
     assert lib.fattn_fwd(a, a, a, a, a, 0, 1, 128, 128, 0.1, 0, None) == 1
     assert lib.fattn_fwd(a, a, a, a, a, 1, 1, 128, 128, 0.0, 0, None) == 1
     assert lib.fattn_fwd(a, a, a, a, a, 1 << 16, 1 << 16, 1, 64, 0.1, 0, None) == 1
-    assert lib.fattn_bwd(a, a, a, a, a, a, a, a, a, 1, 1, 128, 128, 0.1, 1, None, 0, None) == 4
     assert lib.fattn_bwd(a, a, a, a, a, a, a, a, a, 1, 1, 128, 128, 0.1, 1, a + 16, 1 << 30,
                          None) == 4
     assert lib.fattn_bwd(a, a, a, a, a, a, a, a, a, 1, 1, 128, 128, 0.1, 1, a, 16, None) == 4
@@ -111,3 +120,31 @@ def test_host_staged_argument_checks_before_any_device_call(lib):
     # a chunk larger than B*H is clipped to B*H
     assert fattn.fattn_fwd_bwd_host_workspace_bytes(1, 4, 256, 64, 9) == \
         fattn.fattn_fwd_bwd_host_workspace_bytes(1, 4, 256, 64, 4)
+
+
+def test_null_workspace_passes_validation(lib):
+    """A NULL workspace asks for stream-ordered scratch: the arguments pass, and
+    the call proceeds to the device (without one: FATTN_ERR_CUDA)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("needs a machine without a GPU")
+    a = 1 << 20
+    assert lib.fattn_bwd(a, a, a, a, a, a, a, a, a, 1, 1, 128, 128, 0.1, 1, None, 0, None) == 3
+    # validation still comes first
+    assert lib.fattn_bwd(a, a, a, a, a, a, a, a, a, 1, 1, 128, 96, 0.1, 1, None, 0, None) == 2
+
+
+def test_noalloc_checks_arguments_like_fattn_bwd(lib):
+    a = 1 << 20
+    # B = 0 with an unsupported d: the size check comes first, as in fattn_bwd
+    for fn in ("fattn_bwd_noalloc",):
+        f = getattr(lib, fn)
+        assert f(a, a, a, a, a, a, a, a, a, 0, 1, 128, 32, 0.1, 1, None) == 1
+        # a bad scale on a problem beyond the built-in scratch: INVALID_ARG, not WORKSPACE
+        assert f(a, a, a, a, a, a, a, a, a, 1, 8, 16384, 128, float("nan"), 1, None) == 1
+        assert f(a, a, a, a, a, a, a, a, a, 1, 8, 16384, 128, -1.0, 1, None) == 1
+        assert f(a, a, a, a, a, a, a, a, a, 1, 1, 128, 96, 0.1, 1, None) == 2
+        assert f(a, a, a, a, a, a, a, a, a, 1, 8, 16384, 128, 0.1, 1, None) == 4
+    big = (1 << 16, 1 << 16, 1)
+    assert lib.fattn_bwd_noalloc(a, a, a, a, a, a, a, a, a, *big, 64, 0.1, 0, None) == 1
+    assert lib.fattn_bwd(a, a, a, a, a, a, a, a, a, *big, 64, 0.1, 0, a, 1 << 40, None) == 1

@@ -2,14 +2,16 @@
 
 The GPU backward consumes the GPU forward's O and LSE (as a user would);
 the oracle recomputes everything from Q, K, V, dO in fp64.  Bar: dQ, dK, dV
-max-abs <= 2e-2 and mean-abs <= 2e-3.  Small problems are compared element
-by element; the full-size workloads run in the benchmark's launch
-configuration and are compared on whole sampled heads.
+max-abs <= 2e-2 and mean-abs <= 2e-3.  Every workload is compared element
+by element on every head, at full size, in the launch configuration the
+benchmark times; the long-sequence workload's backward is checked on its
+B=1 H=1 N=4096 slice, as the workload defines.
 """
 import numpy as np
 import pytest
 import torch
 
+import bwd_precision_model
 import oracle
 from online_softmax_08_gb300 import fattn
 from online_softmax_08_gb300.inputs import WORKLOADS, default_scale, make_inputs
@@ -68,20 +70,24 @@ def test_backward_matches_oracle_elementwise(B, H, N, d, causal):
 
 def test_backward_logit_stress_small():
     """Q ~ 4 N(0,1): the logit-stress inputs (a forward-only workload) pushed
-    through the backward too.  dK = scale dS^T Q then sums bf16-rounded dS
-    against |Q| up to ~16: rounding dS alone to bf16 (in fp64 otherwise) moves
-    dK by up to 0.035 on these inputs, and the fp32 P and LSE of the kernels
-    flip a few more of those roundings (observed up to 0.045), so the max bar
-    here is 6e-2; the mean bar is the workload's 2e-3."""
+    through the backward too.  dK = scale dS^T Q then reaches |dK| ~ 10, where
+    one bf16 step is 0.0625, so the workloads' absolute 2e-2 bar cannot hold.
+    The bar is derived instead from a CPU model of the kernel's number formats
+    (tests/bwd_precision_model.py: bf16 P and dS, fp32 sums, bf16 outputs) on
+    these same inputs: the model's error against the oracle plus the spread of
+    valid fp32 evaluations and the final half-ulp rounding.  The mean bar is
+    the workloads' 2e-3."""
     q, k, v, do = make_inputs(1, 2, 500, 128, seed=91, q_std=4.0, v_dist="uniform", with_do=True)
     scale = default_scale(128)
     dq, dk, dv = _gpu_grads(q, k, v, do, scale, False)
-    ref = oracle.attention_bwd(_f64(q), _f64(k), _f64(v), _f64(do), scale, False)
-    for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+    qf, kf, vf, dof = _f64(q), _f64(k), _f64(v), _f64(do)
+    ref = oracle.attention_bwd(qf, kf, vf, dof, scale, False)
+    bars, _ = bwd_precision_model.derived_bars(qf, kf, vf, dof, scale, False, ref)
+    for name, got, r, bar in zip(("dq", "dk", "dv"), (dq, dk, dv), ref, bars):
         got = _f64(got)
         assert np.isfinite(got).all()
         err = np.abs(got - r)
-        assert err.max() <= 6e-2, (name, err.max())
+        assert err.max() <= bar, (name, err.max(), bar)
         assert err.mean() <= G_MEAN, (name, err.mean())
 
 
@@ -103,30 +109,67 @@ def test_workspace_contents_do_not_matter():
         _check(_f64(got), r, name)
 
 
-def _sampled_heads(name, causal, n_heads):
+def _all_heads(name, causal, heads_per_call=4):
+    """The workload at full size through the GPU path, then the oracle head by
+    head (a few heads per call, so its N x N fp64 matrices stay bounded) and
+    every element of dQ, dK and dV compared."""
     w = WORKLOADS[name]
     B, H, N, d = w["B"], w["H"], w["N"], w["d"]
     q, k, v, do = make_inputs(B, H, N, d, w["seed"], w["q_std"], w["v_dist"], with_do=True)
     scale = default_scale(d)
-    dq, dk, dv = _gpu_grads(q, k, v, do, scale, causal)
-    g = torch.Generator().manual_seed(w["seed"] + 17)
-    heads = sorted(torch.randperm(B * H, generator=g)[:n_heads].tolist())
-    ref = oracle.attention_bwd(_f64(q), _f64(k), _f64(v), _f64(do), scale, causal, heads=heads)
-    for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
-        _check(_f64(got).reshape(B * H, N, d)[heads], r, name)
+    grads = [_f64(g).reshape(B * H, N, d) for g in _gpu_grads(q, k, v, do, scale, causal)]
+    qf, kf, vf, dof = _f64(q), _f64(k), _f64(v), _f64(do)
+    worst = {n: [0.0, 0.0] for n in ("dq", "dk", "dv")}
+    for h0 in range(0, B * H, heads_per_call):
+        heads = list(range(h0, min(B * H, h0 + heads_per_call)))
+        ref = oracle.attention_bwd(qf, kf, vf, dof, scale, causal, heads=heads)
+        for name, got, r in zip(("dq", "dk", "dv"), grads, ref):
+            g = got[heads]
+            assert np.isfinite(g).all(), name
+            err = np.abs(g - r)
+            worst[name][0] = max(worst[name][0], float(err.max()))
+            worst[name][1] += float(err.sum())
+    for name in worst:
+        mx, total = worst[name][0], worst[name][1] / (B * H * N * d)
+        assert mx <= G_MAX, (name, mx)
+        assert total <= G_MEAN, (name, total)
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_b4h16_n2048_d64_sampled_heads(causal):
-    _sampled_heads("b4h16_n2048_d64", causal, n_heads=4)
+def test_b4h16_n2048_d64_all_heads(causal):
+    _all_heads("b4h16_n2048_d64", causal, heads_per_call=16)
 
 
-def test_headline_b1h32_n8192_d128_causal_sampled_heads():
-    _sampled_heads("b1h32_n8192_d128_causal", True, n_heads=1)
+def test_headline_b1h32_n8192_d128_causal_all_heads():
+    _all_heads("b1h32_n8192_d128_causal", True)
 
 
 def test_long_sequence_backward_slice_b1h1_n4096_d128():
-    _sampled_heads("long_bwd_slice_b1h1_n4096_d128_causal", True, n_heads=1)
+    _all_heads("long_bwd_slice_b1h1_n4096_d128_causal", True)
+
+
+def test_null_workspace_uses_stream_ordered_scratch():
+    """workspace = NULL: the library takes its scratch from the stream-ordered
+    allocator.  dK and dV equal the caller-workspace call bit for bit; dQ's fp32
+    partials are summed in a varying order, so it is compared with the oracle."""
+    q, k, v, do = make_inputs(2, 3, 700, 128, seed=93, with_do=True)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    scale = default_scale(128)
+    o, lse = fattn.forward(qd, kd, vd, scale, True)
+    g_ws = fattn.backward(qd, kd, vd, o, lse, dod, scale, True)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        g_null = fattn.backward(qd, kd, vd, o, lse, dod, scale, True, workspace="stream",
+                                stream=side)
+    side.synchronize()
+    torch.cuda.synchronize()
+    assert fattn.fattn_device_error() == 0
+    assert torch.equal(g_ws[1], g_null[1]) and torch.equal(g_ws[2], g_null[2])
+    ref = oracle.attention_bwd(_f64(q), _f64(k), _f64(v), _f64(do), scale, True)
+    for name, got, r in zip(("dq", "dk", "dv"), g_null, ref):
+        _check(_f64(got), r, name)
 
 
 def test_backward_argument_checks():

@@ -57,14 +57,30 @@ def test_decode_matches_oracle(B, H, Nq, Nkv, d, causal, n_splits):
     assert np.abs(_f64(lse) - lse_ref).max() <= LSE_MAX
 
 
+def _expected_splits(units, Nq, Nkv, n_splits, n_sm):
+    """The documented rule: a request is capped at one range per 128-key tile;
+    0 asks for about ten waves of CTAs over the device's SMs with at least four
+    tiles per range; empty ranges are dropped."""
+    n_tiles = -(-Nkv // 128)
+    want = n_splits
+    if want <= 0:
+        ctas = units * -(-Nq // 256)
+        want = min(-(-10 * n_sm // ctas), n_tiles // 4)
+    want = max(1, min(want, n_tiles))
+    tps = -(-n_tiles // want)
+    return -(-n_tiles // tps)
+
+
 def test_split_counts():
     lib = fattn.load()
-    # one range per 128-key tile at most; automatic: about ten waves of CTAs,
-    # at least four tiles per range
-    assert lib.fattn_decode_splits(1, 1, 1, 1300, 128, 1000) == 11
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    for args in [(1, 1, 1, 1300, 1000), (1, 1, 1, 1300, 3), (4, 32, 1, 32768, 0),
+                 (1, 1, 1, 1300, 0), (2, 8, 300, 70000, 0), (16, 64, 1, 4096, 0)]:
+        B, H, Nq, Nkv, n = args
+        assert lib.fattn_decode_splits(B, H, Nq, Nkv, 128, n) == \
+            _expected_splits(B * H, Nq, Nkv, n, n_sm), args
+    assert lib.fattn_decode_splits(1, 1, 1, 1300, 128, 1000) == 11  # one range per tile
     assert lib.fattn_decode_splits(1, 1, 1, 1300, 128, 3) == 3
-    assert lib.fattn_decode_splits(4, 32, 1, 32768, 128, 0) == 12
-    assert lib.fattn_decode_splits(1, 1, 1, 1300, 128, 0) == 2
     assert lib.fattn_decode_splits(1, 1, 2, 1, 128, 0) == 0  # Nq > Nkv is invalid
 
 

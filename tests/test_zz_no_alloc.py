@@ -9,13 +9,15 @@ alone in a fresh process.
 
 Checks: two calls in a row through the C-ABI agree with fattn_bwd (the
 entry point that takes a caller workspace) within the parity tolerance of the
-other backward tests; a problem whose workspace exceeds the built-in size is
-rejected before any launch.
+other backward tests; a small call made right after a larger one (so the
+array still holds the larger call's data) matches the fp64 oracle; a problem
+whose workspace exceeds the built-in size is rejected before any launch.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from online_softmax_08_gb300 import fattn
 from online_softmax_08_gb300.inputs import default_scale, make_inputs
 
@@ -49,6 +51,39 @@ def test_noalloc_matches_workspace_backward_twice(B, H, N, d, causal):
             err = np.abs(_f64(got) - _f64(want))
             assert err.max() <= G_MAX and err.mean() <= G_MEAN
     assert fattn.fattn_device_error() == 0
+
+
+def _noalloc(q, k, v, o, lse, do, scale, causal):
+    B, H, N, d = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    status = fattn.load().fattn_bwd_noalloc(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale, int(causal),
+        torch.cuda.current_stream().cuda_stream)
+    assert status == 0, fattn.fattn_status_string(status)
+    return dq, dk, dv
+
+
+@pytest.mark.gpu
+def test_noalloc_after_a_larger_call_matches_the_oracle():
+    """A ragged small problem right after a large one that filled much of the
+    array: the stale contents must not leak into the small call's results."""
+    dev = torch.device("cuda:0")
+    big = [x.to(dev) for x in make_inputs(1, 8, 4000, 128, seed=6161, with_do=True)]
+    scale = default_scale(128)
+    o, lse = fattn.forward(*big[:3], scale, True)
+    _noalloc(*big[:3], o, lse, big[3], scale, True)
+    q, k, v, do = make_inputs(1, 1, 777, 128, seed=6162, with_do=True)
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    o, lse = fattn.forward(qd, kd, vd, scale, True)
+    got = _noalloc(qd, kd, vd, o, lse, dod, scale, True)
+    torch.cuda.synchronize()
+    assert fattn.fattn_device_error() == 0
+    f64 = lambda t: t.detach().to("cpu", torch.float64).numpy()
+    ref = oracle.attention_bwd(f64(q), f64(k), f64(v), f64(do), scale, True)
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        err = np.abs(f64(g) - r)
+        assert err.max() <= G_MAX and err.mean() <= G_MEAN, (name, err.max(), err.mean())
 
 
 @pytest.mark.gpu

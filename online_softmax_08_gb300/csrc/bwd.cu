@@ -35,10 +35,11 @@
 // after dV(i).  The dQ^T partial of each
 // step is read out of TMEM by a drain warpgroup (freeing Y for dP(i+1)) and
 // added into an fp32 accumulator with bulk tensor reduces of 16 query rows,
-// staged round-robin through NDQ shared-memory buffers so that filling one
+// staged round-robin through four shared-memory buffers so that filling one
 // overlaps the reduces reading the others (two buffers were 11 % faster than
-// one, three 1.2 % faster than two); the drain is busy for the whole step, so
-// these reductions are what bounds the kernel.  The alternative, a second pass parallel over query blocks, would
+// one, three 1.2 % faster than two, four 3.8 % faster than three).  Each SM's
+// bulk-copy unit adds at most about 25 bytes per cycle, and a step hands it
+// 64 KB, so these reductions are what bounds the kernel.  The alternative, a second pass parallel over query blocks, would
 // recompute S and dP (seven matmuls per tile instead of five).
 //
 // Warp roles (512 threads): warps 0-7 form P and dS, warpgroup w for queries
@@ -54,6 +55,20 @@
 namespace fattn {
 namespace {
 
+// Shape of the dQ staging (compile-time, for A/B builds): query rows per bulk
+// reduce, staging buffers, and whether the layout keeps 1 KB of slack to align
+// the dynamic shared memory (0: the kernel requires an aligned base and
+// reports a misaligned one through the error word).
+#ifndef FATTN_DQ_ROWS
+#define FATTN_DQ_ROWS 16
+#endif
+#ifndef FATTN_DQ_BUFS
+#define FATTN_DQ_BUFS 4
+#endif
+#ifndef FATTN_SMEM_SLACK
+#define FATTN_SMEM_SLACK 0
+#endif
+
 template <int D>
 struct Bwd {
   static constexpr int BK = 128;                 // keys per CTA
@@ -68,12 +83,15 @@ struct Bwd {
   static constexpr int OFF_DO = OFF_Q + QST * TILE;            // [OST]
   static constexpr int OFF_DS = OFF_DO + OST * TILE;           // dS^T [128 keys][128 q] bf16
   static constexpr int OFF_STAT = OFF_DS + 2 * HALF;           // [QST] x {-lse2[BQ], delta[BQ]}
-  // dQ staging: NDQ buffers of 16 query rows (fp32), filled round-robin, so that
+  // dQ staging: NDQ buffers of RPC query rows (fp32), filled round-robin, so that
   // NDQ - 1 bulk reduces are in flight while the next buffer is filled
-  static constexpr int NDQ = D == 128 ? 3 : 4;
-  static constexpr int OFF_DQ = OFF_STAT + QST * 2 * BQ * 4;  // fp32 staging [NDQ][16 q][D]
-  static constexpr int OFF_BAR = OFF_DQ + NDQ * 16 * D * 4;
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  static constexpr int RPC = FATTN_DQ_ROWS;
+  static constexpr int NDQ = FATTN_DQ_BUFS;
+  static constexpr int CPS = BQ / RPC;  // chunks per step
+  static constexpr int OFF_DQ = OFF_STAT + QST * 2 * BQ * 4;  // fp32 staging [NDQ][RPC q][D]
+  static constexpr int OFF_BAR = OFF_DQ + NDQ * RPC * D * 4;
+  static constexpr int SLACK = FATTN_SMEM_SLACK;
+  static constexpr int SMEM = OFF_BAR + 256 + SLACK;
   static constexpr int THREADS = 512;
   static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_X = 2 * D, TM_Y = 2 * D + 128;
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BQ, false, false);   // S^T, dP^T
@@ -164,6 +182,10 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
   constexpr int BQ = C::BQ, QST = C::QST, OST = C::OST;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
+  if (C::SLACK < 1023 && (raw & 1023u)) {  // no room to align: report and leave
+    if (threadIdx.x == 0 && p.err) atomicCAS(p.err, 0u, (unsigned)(ERR_SITE_BWD | 0x41));
+    return;
+  }
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw);
 
@@ -422,18 +444,21 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
       mbar_arrive(bar(B_DQ_FREE));
       // lanes are d (lanes >= d are padding), columns are queries: stage 16 query
       // rows at a time in shared memory and add them with one bulk tensor reduce
+      constexpr int RPC = C::RPC;
 #pragma unroll
-      for (int h = 0; h < 8; ++h, ++nbuf) {  // 16 query rows per reduce
-        const uint32_t buf = sdq + (uint32_t)(nbuf % C::NDQ) * (16 * D * 4);
+      for (int h = 0; h < C::CPS; ++h, ++nbuf) {  // RPC query rows per reduce
+        const uint32_t buf = sdq + (uint32_t)(nbuf % C::NDQ) * (RPC * D * 4);
         // the reduce that last read this buffer, NDQ chunks ago, is done reading it
         if (t == 0) bulk_wait_read<C::NDQ - 1>();
         named_bar_sync(2, 128);
         if (t < D) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
+          for (int c = 0; c < RPC; ++c) {
+            const int q = h * RPC + c;  // query column of the dQ^T tile
             asm volatile("st.shared.b32 [%0], %1;" ::"r"(buf + (uint32_t)(c * D + t) * 4u),
-                         "r"(r[h >> 1][(h & 1) * 16 + c])
+                         "r"(r[q >> 5][q & 31])
                          : "memory");
+          }
         }
         fence_proxy_async_smem();
         named_bar_sync(2, 128);
@@ -441,7 +466,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
           // rows past the sequence end belong to the next one (or lie past the
           // tensor, where TMA clips them): their partial is exactly zero, since
           // their LSE is +inf, so adding it changes nothing
-          tma_reduce_add_3d(&tm_dq, buf, 0, row0 + q0 + 16 * h, bh);
+          tma_reduce_add_3d(&tm_dq, buf, 0, row0 + q0 + RPC * h, bh);
           bulk_commit();
         }
       }
@@ -667,6 +692,8 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
 }
 
 }  // namespace
+
+int bwd_dq_rows() { return FATTN_DQ_ROWS; }
 
 cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,

@@ -159,6 +159,9 @@ cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
                             const CUtensorMap& tdk, const CUtensorMap& tdv,
                             const CUtensorMap& tdq_acc, const BwdParams& p, cudaStream_t stream);
+// Query rows per bulk reduce of the backward's dQ partials (the box height of
+// the accumulator's tensor map).
+int bwd_dq_rows();
 cudaError_t launch_bwd_convert(const float* dq_acc, void* dq, long long n, float scale,
                                int n_sm, cudaStream_t stream);
 

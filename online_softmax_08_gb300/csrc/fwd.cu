@@ -24,9 +24,11 @@
 //              softmax's packed f32x2 arithmetic spilled.
 //
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 after it.
-// P_s (bf16, two per 32-bit column) overwrites the first 64 columns of S_s
-// once the softmax has read S_s, and feeds O_s += P_s V as the TMEM A operand,
-// so P never touches shared memory.  The softmax releases P_s in two halves of
+// At d = 128, P_s (bf16, two per 32-bit column) overwrites the first 64 columns
+// of S_s once the softmax has read S_s, and feeds O_s += P_s V as the TMEM A
+// operand, so P never touches shared memory.  At d = 64, P_0 and P_1 have 64
+// columns each after O_1, so S_s = Q_s K_{j+1}^T is issued as soon as the
+// softmax has S_s(j) in registers (B_S_READ) and runs while it forms P_s(j).  The softmax releases P_s in two halves of
 // 64 keys, and the MMA thread issues the half of O_s += P_s V_j over the first
 // half while the softmax forms the second; per subtile it issues all of
 // O_s += P_s V_j before S_s = Q_s K_{j+1}^T (the pipe runs them in order).
@@ -35,6 +37,12 @@
 #define FATTN_INLINE_WAIT_SLOW_PATH
 #include "common.cuh"
 #include "ptx.cuh"
+
+// Built with FATTN_FWD_DEC64=0 the d = 64 kernel keeps P over S as at d = 128
+// (kept buildable for A/B timing).
+#ifndef FATTN_FWD_DEC64
+#define FATTN_FWD_DEC64 1
+#endif
 
 namespace fattn {
 namespace {
@@ -94,6 +102,14 @@ struct Fwd {
   static_assert((2 * REG_SOFTMAX + REG_CTRL) * 128 <= THREADS * REG_LAUNCH, "register split");
   static constexpr uint32_t TM_S = 0;
   static constexpr uint32_t TM_O = 256;
+  // d = 64 leaves 128 TMEM columns free: P_s gets a region of its own there
+  // (64 columns of bf16 pairs per subtile), so S_s = Q_s K_{j+1}^T can be
+  // issued as soon as the softmax has read S_s(j) into registers, instead of
+  // after O_s += P_s V_j; the softmax then never waits on its own subtile's MMAs
+  static constexpr bool DEC = D == 64 && FATTN_FWD_DEC64 != 0;
+  static constexpr uint32_t TM_P = DEC ? TM_O + 2 * D : TM_S;  // P_s at TM_P + (DEC ? 64 : 128) s
+  static constexpr uint32_t P_STRIDE = DEC ? 64 : 128;
+  static_assert(!DEC || TM_P + 2 * 64 <= 512, "TMEM budget");
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
 };
@@ -106,8 +122,12 @@ enum {
   B_PV_DONE = 5,  // [2] MMA -> epilogue: O_s += P_s V finished
   B_P_HALF = 7,   // [2] softmax -> MMA: keys 0-63 of P_s in TMEM and O_s rescaled
   B_MMA_DONE = 9,
-  B_KV_FULL = 10,  // [STAGES], then kv_empty [STAGES]
+  B_S_READ = 10,  // [2] softmax -> MMA (d = 64): S_s is in registers, its TMEM may be rewritten
+  B_KV_FULL = 12,  // [STAGES], then kv_empty [STAGES]
 };
+// the barriers, the TMEM address slot and the abort flag share 256 bytes
+static_assert(8 * (B_KV_FULL + 2 * Fwd<64>::STAGES) + 8 <= 256, "barrier block");
+static_assert(8 * (B_KV_FULL + 2 * Fwd<128>::STAGES) + 8 <= 256, "barrier block");
 
 // VARLEN: the CTA's sequence comes from p.vl.cu_seqlens (packed head-major
 // rows); otherwise the dense [B, H, N, d] layout.  SPLIT (dense only): the CTA
@@ -191,6 +211,7 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
       mbar_init(bar(B_P_FULL + s), 128);
       mbar_init(bar(B_P_HALF + s), 128);
       mbar_init(bar(B_PV_DONE + s), 1);
+      mbar_init(bar(B_S_READ + s), 128);
     }
     mbar_init(bar(B_MMA_DONE), 1);
     for (int i = 0; i < ST; ++i) {
@@ -272,7 +293,7 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
 #pragma unroll
         for (int k = 0; k < C::BN / 32; ++k) {  // 16 keys = 8 packed TMEM columns per step
           const int kk = half * (C::BN / 32) + k;
-          mma_bf16_ts_w(tmem + C::TM_O + s * D, tmem + C::TM_S + s * 128 + kk * 8,
+          mma_bf16_ts_w(tmem + C::TM_O + s * D, tmem + C::TM_P + s * C::P_STRIDE + kk * 8,
                       sdesc_sw128(b + kk * 16 * 128, C::HALF, 1024), C::IDESC_PV,
                       (j > 0 || kk > 0));
         }
@@ -289,7 +310,42 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
           mma_commit_w(kv_empty0 + 8u * 0);
         }
       }
-      for (int j = 0; ok && j < n_max; ++j) {
+      for (int j = 0; C::DEC && ok && j < n_max; ++j) {
+        // S_s(j + 1) once the softmax holds S_s(j) in registers; O_s += P_s V_j
+        // once P_s(j) is in its own region.  The pipe runs them in issue order.
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          if (ok && j + 1 < nt[s]) {
+            ok = kv_wait(2 * (j + 1)) &&
+                 __all_sync(0xffffffffu, mbar_wait(bar(B_S_READ + s), j & 1, wctx, ERR_SITE_FWD | 0x19));
+            if (ok) {
+              tc_fence_after();
+              issue_s(s, j + 1);
+            }
+          }
+        }
+        if (!ok) break;
+        if (j + 1 < n_max) mma_commit_w(kv_empty0 + 8u * ((2 * (j + 1)) % ST));
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          if (ok && j < nt[s]) {
+            ok = kv_wait(2 * j + 1) &&
+                 __all_sync(0xffffffffu, mbar_wait(bar(B_P_HALF + s), j & 1, wctx, ERR_SITE_FWD | 0x18));
+            if (ok) {
+              tc_fence_after();
+              issue_pv(s, j, 0);
+              ok = __all_sync(0xffffffffu, mbar_wait(bar(B_P_FULL + s), j & 1, wctx, ERR_SITE_FWD | 0x14));
+            }
+            if (ok) {
+              tc_fence_after();
+              issue_pv(s, j, 1);
+            }
+          }
+        }
+        if (!ok) break;
+        mma_commit_w(kv_empty0 + 8u * ((2 * j + 1) % ST));
+      }
+      for (int j = 0; !C::DEC && ok && j < n_max; ++j) {
         const bool next = j + 1 < n_max;
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
@@ -332,13 +388,16 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::TM_S + s * 128;
     const uint32_t tO = tmem + lane_off + C::TM_O + s * D;
+    const uint32_t tP = tmem + lane_off + C::TM_P + s * C::P_STRIDE;
     const int row = my_r0 + t;
     const float sl2 = p.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     unsigned long long n_full = 0, n_masked = 0;
 
     for (int j = 0; j < my_nt; ++j) {
-      // s_full also means every earlier MMA, including O_s += P_s V_{j-1}, is done
+      // s_full also means every earlier MMA is done; at d = 128 that includes
+      // O_s += P_s V_{j-1}, issued before S_s(j).  At d = 64 S_s(j) is issued
+      // first, and the softmax waits for PV_DONE before it touches O_s or P_s.
       mbar_wait(bar(B_S_FULL + s), j & 1, wctx, ERR_SITE_FWD | 0x21);
       tc_fence_after();
       uint32_t u[4][32];
@@ -353,6 +412,10 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
       for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(u[c][i]);
+      if (C::DEC) {  // S_s is in registers: its TMEM may take S_s(j + 1)
+        tc_fence_before();
+        mbar_arrive(bar(B_S_READ + s));
+      }
 
       // masks go in before the block maximum
       const int c0 = (jlo + j) * C::BN;
@@ -407,7 +470,12 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
           pk[k / 2] = pack_bf16x2(p0, p1);
           pk[k / 2 + 1] = pack_bf16x2(p2, p3);
         }
-        tmem_st32(tS + h * 32, pk);
+        if (C::DEC && h == 0 && j > 0) {
+          // O_s += P_s V_{j-1} has finished: P_s's region is free and O_s complete
+          mbar_wait(bar(B_PV_DONE + s), (j - 1) & 1, wctx, ERR_SITE_FWD | 0x25);
+          tc_fence_after();
+        }
+        tmem_st32(tP + h * 32, pk);
         if (h == 0) {
           // O_s is rescaled before the first half of PV adds into it (the scores of
           // the first half are no longer needed, which leaves the registers for it)

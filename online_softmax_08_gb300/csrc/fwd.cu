@@ -1,12 +1,12 @@
 // fwd.cu -- FlashAttention forward for sm_103a (tcgen05 + TMEM + TMA).
 //
 // One CTA owns 256 query rows of one (batch, head): two 128-row subtiles
-// Q_0, Q_1 ("In a real kernel this loop runs for a whole tile of queries at
-// once", tm_flash_attention_math, "The block-wise update, and the full
-// algorithm").  K/V tiles of 128 keys stream through a ring of shared-memory
-// slots filled by TMA; the score tile S = Q K^T lives only in TMEM
-// ("A score tile is temporary state", page "FlashAttention tiles exact
-// softmax without materializing the score matrix").
+// Q_0, Q_1, each running the single-query recurrence of "tm_flash_attention_math"
+// ("The block-wise update, and the full algorithm") for all of its rows at
+// once.  K/V tiles of 128 keys stream through a ring of shared-memory slots
+// filled by TMA; the score tile S = Q K^T lives only in TMEM ("A score tile is
+// temporary state", page "FlashAttention tiles exact softmax without
+// materializing the score matrix").
 //
 // Warp roles (384 threads):
 //   warps 0-3  softmax for Q_0, warps 4-7 softmax for Q_1: thread t owns query

@@ -10,9 +10,9 @@
  *
  *   S = Q K^T * scale           "FlashAttention tiles exact softmax..." (page 1),
  *                               opening equations; "tm_flash_attention_math"
- *                               (page 3), "What we must compute"
+ *                               (page 3), "What we must compute, and why storage is the problem"
  *   P = softmax(S) by rows      three-pass safe softmax: max, sum, normalise
- *                               (page 3, "Safe softmax: the max-subtraction")
+ *                               (page 3, "Safe softmax: the max-subtraction we cannot give up")
  *   O = P V,  LSE = m + ln l    the per-row statistic the backward pass keeps
  *                               ("Decoding flash attention", "The backward pass")
  *
@@ -255,8 +255,9 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v, const dou
 /* Tile classification of one head's (query tile, key tile) grid, by brute
  * enumeration.  Query tiles hold rows [i0, min(i0+block_q, N) - 1], key tiles
  * columns [j0, min(j0+block_k, N) - 1].  A tile is
- *   skipped iff causal and j0 > i_max (wholly above the diagonal: page 1,
- *           "Tiles entirely beyond the permitted region can be skipped"),
+ *   skipped iff causal and j0 > i_max (wholly above the diagonal, so no key of
+ *           it is visible: page 1, "Causal masking fits inside the tiled
+ *           computation"),
  *   masked  iff not skipped and (causal and j_max > i0, i.e. it crosses the
  *           diagonal, or it runs past N, the ragged last key tile),
  *   full    otherwise.

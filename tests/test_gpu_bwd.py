@@ -13,6 +13,7 @@ import torch
 
 import bwd_precision_model
 import oracle
+import parity_report
 from online_softmax_08_gb300 import fattn
 from online_softmax_08_gb300.inputs import WORKLOADS, default_scale, make_inputs
 
@@ -83,6 +84,10 @@ def test_backward_logit_stress_small():
     qf, kf, vf, dof = _f64(q), _f64(k), _f64(v), _f64(do)
     ref = oracle.attention_bwd(qf, kf, vf, dof, scale, False)
     bars, _ = bwd_precision_model.derived_bars(qf, kf, vf, dof, scale, False, ref)
+    parity_report.record("logit stress B1 H2 N500 d128 bwd (derived bars %s)"
+                         % ", ".join("%.3g" % b for b in bars),
+                         **{n: (np.abs(_f64(g) - r).max(), np.abs(_f64(g) - r).mean())
+                            for n, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref)})
     for name, got, r, bar in zip(("dq", "dk", "dv"), (dq, dk, dv), ref, bars):
         got = _f64(got)
         assert np.isfinite(got).all()
@@ -113,7 +118,8 @@ def _all_heads(name, causal, heads_per_call=4):
     """The workload at full size through the GPU path, then the oracle head by
     head (a few heads per call, so its N x N fp64 matrices stay bounded) and
     every element of dQ, dK and dV compared."""
-    w = WORKLOADS[name]
+    workload = name
+    w = WORKLOADS[workload]
     B, H, N, d = w["B"], w["H"], w["N"], w["d"]
     q, k, v, do = make_inputs(B, H, N, d, w["seed"], w["q_std"], w["v_dist"], with_do=True)
     scale = default_scale(d)
@@ -129,6 +135,8 @@ def _all_heads(name, causal, heads_per_call=4):
             err = np.abs(g - r)
             worst[name][0] = max(worst[name][0], float(err.max()))
             worst[name][1] += float(err.sum())
+    parity_report.record("%s %s bwd, all heads" % (workload, "causal" if causal else "non-causal"),
+                         **{n: (v[0], v[1] / (B * H * N * d)) for n, v in worst.items()})
     for name in worst:
         mx, total = worst[name][0], worst[name][1] / (B * H * N * d)
         assert mx <= G_MAX, (name, mx)

@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import oracle
+import parity_report
 from online_softmax_08_gb300 import fattn
 from online_softmax_08_gb300.inputs import WORKLOADS, default_scale, make_inputs, sample_rows
 
@@ -33,8 +34,11 @@ def _run(q, k, v, scale, causal, counts=False):
     return o, lse, (tc.cpu().tolist() if counts else None)
 
 
-def _check(o_gpu, lse_gpu, o_ref, lse_ref):
+def _check(o_gpu, lse_gpu, o_ref, lse_ref, case=None):
     err = np.abs(o_gpu - o_ref)
+    if case:
+        parity_report.record(case, o=(err.max(), err.mean()),
+                             lse=np.abs(lse_gpu - lse_ref).max())
     assert np.isfinite(o_gpu).all() and np.isfinite(lse_gpu).all()
     assert err.max() <= O_MAX, err.max()
     assert err.mean() <= O_MEAN, err.mean()
@@ -81,7 +85,7 @@ def test_single_head_workload_full():
     scale = default_scale(w["d"])
     o, lse, _ = _run(q, k, v, scale, False)
     o_ref, lse_ref = oracle.attention_fwd(_f64(q), _f64(k), _f64(v), scale, False)
-    _check(_f64(o), _f64(lse), o_ref, lse_ref)
+    _check(_f64(o), _f64(lse), o_ref, lse_ref, case="single_head_n256_d64 fwd")
 
 
 def test_logit_stress_small_elementwise():
@@ -140,6 +144,8 @@ def _all_heads(name, causal, heads_per_call=8):
         err = np.abs(o[h0:h1] - o_ref[0])
         o_max, o_sum = max(o_max, float(err.max())), o_sum + float(err.sum())
         lse_max = max(lse_max, float(np.abs(lse[h0:h1] - lse_ref[0]).max()))
+    parity_report.record("%s %s fwd, all heads" % (name, "causal" if causal else "non-causal"),
+                         o=(o_max, o_sum / o.size), lse=lse_max)
     assert o_max <= O_MAX, o_max
     assert o_sum / o.size <= O_MEAN, o_sum / o.size
     assert lse_max <= LSE_MAX, lse_max
@@ -154,7 +160,8 @@ def _rows_of_every_head(name, causal, n_rows=64):
     o_ref, lse_ref = oracle.attention_fwd_rows(qf, kf, vf, scale, causal, bh, rr)
     o_gpu = o.reshape(B * H, N, d)[bh, rr]
     lse_gpu = lse.reshape(B * H, N)[bh, rr]
-    _check(o_gpu, lse_gpu, o_ref, lse_ref)
+    _check(o_gpu, lse_gpu, o_ref, lse_ref,
+           case="%s fwd, %d rows of every head" % (name, len(rows)))
 
 
 @pytest.mark.parametrize("causal", [False, True])

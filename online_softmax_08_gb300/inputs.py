@@ -68,12 +68,15 @@ def workload_inputs(name, with_do=False, **override):
 
 
 def sample_rows(N, count, seed, always=(0, 127, 128)):
-    """Seeded query-row sample: the listed rows, N-1, then uniform draws."""
+    """Seeded query-row sample of min(count, N) distinct rows: the listed rows,
+    N-1, then uniform draws (repeated draws are drawn again)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
-    rows = [r for r in always if r < N] + [N - 1]
-    extra = torch.randint(0, N, (max(0, count - len(rows)),), generator=g).tolist()
-    return sorted(set(rows + extra))
+    rows = set(r for r in always if r < N) | {N - 1}
+    count = min(count, N)
+    while len(rows) < count:
+        rows.update(torch.randint(0, N, (count - len(rows),), generator=g).tolist())
+    return sorted(rows)[:count] if len(rows) > count else sorted(rows)
 
 
 def make_varlen_inputs(lengths, H, d, seed, with_do=False):

@@ -345,15 +345,19 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
         if (!ok) break;
         mma_commit_w(kv_empty0 + 8u * ((2 * j + 1) % ST));
       }
+      // each K/V tile is waited for once per iteration, not once per subtile: a
+      // satisfied wait still costs this warp tens of cycles, during which the
+      // tensor pipe may run dry
       for (int j = 0; !C::DEC && ok && j < n_max; ++j) {
         const bool next = j + 1 < n_max;
+        bool k_next = false;      // K_{j+1} waited for
+        ok = kv_wait(2 * j + 1);  // V_j: some subtile has tile j
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           const int nts = s ? nt1 : nt0;
           if (ok && j < nts) {
             // the first half of PV runs while the softmax forms the second half of P
-            ok = kv_wait(2 * j + 1) &&
-                 __all_sync(0xffffffffu, mbar_wait(bar(B_P_HALF + s), j & 1, wctx, ERR_SITE_FWD | 0x18));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_P_HALF + s), j & 1, wctx, ERR_SITE_FWD | 0x18));
             if (ok) {
               tc_fence_after();
               issue_pv(s, j, 0);
@@ -365,7 +369,10 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
             }
           }
           if (ok && j + 1 < nts) {  // after the PV above: S_s is overwritten in pipe order
-            ok = kv_wait(2 * (j + 1));
+            if (!k_next) {
+              ok = kv_wait(2 * (j + 1));
+              k_next = true;
+            }
             if (ok) issue_s(s, j + 1);
           }
         }

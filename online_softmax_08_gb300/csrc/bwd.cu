@@ -106,6 +106,11 @@ struct Bwd {
   __host__ __device__ static constexpr uint32_t p_col(int kk) {
     return TM_X + 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3);
   }
+  // the same for the packed dS^T that dK reads: each warpgroup writes it over the
+  // first half of the dP^T columns it has read, Y + 64w
+  __host__ __device__ static constexpr uint32_t ds_col(int kk) {
+    return TM_Y + 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3);
+  }
 };
 
 // Every barrier is waited on by parity, so no waiter may fall two phases
@@ -115,9 +120,9 @@ enum {
   B_KV = 0,
   B_S_FULL = 1,     // MMA -> compute warps: S^T in X
   B_P_FULL = 2,     // compute warps -> MMA: P^T (bf16) in X, S^T read
-  B_DS_HALF = 3,    // compute warps -> MMA: the first 32 queries of each half of dS^T stored
+  B_DS_HALF = 3,    // compute warps -> MMA: the first 32 queries of each half of dS^T in TMEM
   B_DP_FULL = 4,    // MMA -> compute warps: dP^T in Y
-  B_DS_FULL = 5,    // compute warps -> MMA: dS^T in shared memory, dP^T read
+  B_DS_FULL = 5,    // compute warps -> MMA: dS^T in TMEM and shared memory, dP^T read
   B_DS_FREE = 6,    // MMA -> compute warps: dK and dQ have read dS^T
   B_DQ_FULL = 7,    // MMA -> drain: dQ^T in Y
   B_DQ_FREE = 8,    // drain -> MMA: dQ^T read, Y may be overwritten
@@ -348,15 +353,16 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
                         sdesc_sw128(sdo + kk * 16 * 128, C::HALF, 1024), C::IDESC_ACC,
                         (acc || kk > 0));
       };
-      // dK += dS^T (K-major) * Q (MN-major), over the 16-query steps kk of one
-      // pass: pass 0 takes queries 0-31 of each 64-query half (kk = 0, 1, 4, 5),
-      // pass 1 queries 32-63 (kk = 2, 3, 6, 7), as the compute warps store them
+      // dK += dS^T (TMEM, over dP^T in Y) * Q (MN-major), over the 16-query steps kk
+      // of one pass: pass 0 takes queries 0-31 of each 64-query half (kk = 0, 1, 4,
+      // 5), pass 1 queries 32-63 (kk = 2, 3, 6, 7), as the compute warps store them.
+      // With A in TMEM the MMA reads only Q from shared memory, whose bandwidth the
+      // step's MMAs, TMA loads, dS stores and dQ reduces share
       auto mma_dk = [&](uint32_t sq, bool acc, int pass) {
 #pragma unroll
         for (int j = 0; j < BQ / 32; ++j) {
           const int kk = (j >> 1) * 4 + pass * 2 + (j & 1);
-          const uint32_t ao = (kk >> 2) * C::HALF + (kk & 3) * 32;
-          mma_bf16_ss_w(tmem + C::TM_DK, sdesc_sw128(sDS + ao, 16, 1024),
+          mma_bf16_ts_w(tmem + C::TM_DK, tmem + C::ds_col(kk),
                         sdesc_sw128(sq + kk * 16 * 128, C::HALF, 1024), C::IDESC_ACC,
                         (acc || kk > 0));
         }
@@ -570,23 +576,28 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
                      __uint_as_float(u[c][i + 2]), __uint_as_float(u[c][i + 3]), d4.z, d4.w,
                      ds[i + 2], ds[i + 3]);
         }
+        uint32_t dpk[16];  // bf16 pairs of queries (2e, 2e + 1)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) dpk[e] = pack_bf16x2(ds[2 * e], ds[2 * e + 1]);
+        // for dK: into TMEM over the dP^T columns already read (Y + 64w + 16c)
+        tmem_st16(tY + 16 * c, dpk);
+        // for dQ: into shared memory, MN-major
 #pragma unroll
         for (int e = 0; e < 4; ++e) {  // four 16-byte chunks of 8 queries
           const int chunk = c * 4 + e;
           st_shared_v4(sbase + C::OFF_DS + w * C::HALF + t * 128 + ((chunk ^ (t & 7)) << 4),
-                       pack_bf16x2(ds[e * 8], ds[e * 8 + 1]),
-                       pack_bf16x2(ds[e * 8 + 2], ds[e * 8 + 3]),
-                       pack_bf16x2(ds[e * 8 + 4], ds[e * 8 + 5]),
-                       pack_bf16x2(ds[e * 8 + 6], ds[e * 8 + 7]));
+                       dpk[4 * e], dpk[4 * e + 1], dpk[4 * e + 2], dpk[4 * e + 3]);
         }
-        if (c == 0) {  // the first pass's dS^T is in shared memory: dK can start on it
-          fence_proxy_async_smem();
+        if (c == 0) {  // the first pass's dS^T is in TMEM: dK can start on it
+          tmem_wait_st();
+          tc_fence_before();
           mbar_arrive(bar(B_DS_HALF));
         }
       }
       mbar_arrive(bar(B_Q_EMPTY + st));  // LSE2 and D of this stage are no longer read
       fence_proxy_async_smem();
-      tc_fence_before();  // the dP^T reads of Y precede dQ^T written into it
+      tmem_wait_st();
+      tc_fence_before();  // the dP^T reads and dS^T writes of Y precede dQ^T written into it
       mbar_arrive(bar(B_DS_FULL));
       if (it + 1 < n_it) form_p(it + 1);
     }

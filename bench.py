@@ -121,9 +121,12 @@ def barrier(world):
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """nvidia-smi samples of SM clock and throttle reasons while running.  Each
+    sample carries nvidia-smi's timestamp; the figures are taken from the samples
+    that fall inside the timed region (region_start .. region_end), or from all
+    samples when the region is shorter than the sampling interval."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -131,6 +134,15 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.t_start = self.t_end = None
+
+    def region_start(self):
+        import datetime
+        self.t_start = datetime.datetime.now()
+
+    def region_end(self):
+        import datetime
+        self.t_end = datetime.datetime.now()
 
     def start(self):
         try:
@@ -155,23 +167,32 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        samples = []  # (time or None, sm MHz, max MHz, active reasons)
         for ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                sm, smax = float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+            try:
+                when = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                when = None
+            active = {name for name, val in zip(names, parts[6:10]) if val.lower().startswith("active")}
+            samples.append((when, sm, smax, active))
+        inside = [x for x in samples
+                  if x[0] is not None and self.t_start is not None and self.t_end is not None
+                  and self.t_start <= x[0] <= self.t_end]
+        use = inside or samples
+        reasons = set().union(*(x[3] for x in use)) if use else set()
+        return {"sm_mhz": statistics.median(x[1] for x in use) if use else None,
+                "sm_max_mhz": max(x[2] for x in use) if use else None,
+                "reasons": sorted(reasons), "samples": len(samples),
+                "samples_in_timed_region": len(inside)}
 
 
 # ------------------------------------------------------------------ reference arm / CPU baseline
@@ -310,11 +331,13 @@ def run_gpu(args):
     barrier(world)
     torch.cuda.synchronize(device)
     t0, t1 = ev(), ev()
+    clocks.region_start()
     t0.record(stream)
     for i in range(K):
         step(i)
     t1.record(stream)
     torch.cuda.synchronize(device)
+    clocks.region_end()
     barrier(world)
     clk = clocks.stop()
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, device)
@@ -489,11 +512,13 @@ def run_gpu_varlen(args):
     time.sleep(0.3)
     torch.cuda.synchronize(device)
     t0, t1 = ev(), ev()
+    clocks.region_start()
     t0.record(stream)
     for i in range(K):
         step(i)
     t1.record(stream)
     torch.cuda.synchronize(device)
+    clocks.region_end()
     clk = clocks.stop()
     assert fattn.fattn_device_error() == 0, "an in-kernel wait timed out"
     ms = t0.elapsed_time(t1) / K
@@ -554,11 +579,13 @@ def run_gpu_decode(args):
     time.sleep(0.3)
     K = args.steps
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.region_start()
     t0.record(stream)
     for _ in range(K):
         step()
     t1.record(stream)
     torch.cuda.synchronize(device)
+    clocks.region_end()
     clk = clocks.stop()
     assert fattn.fattn_device_error() == 0, "an in-kernel wait timed out"
     ms = t0.elapsed_time(t1) / K
@@ -607,11 +634,13 @@ def run_gpu_softmax(args):
     time.sleep(0.3)
     K = args.steps
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.region_start()
     t0.record(stream)
     for _ in range(K):
         step()
     t1.record(stream)
     torch.cuda.synchronize(device)
+    clocks.region_end()
     clk = clocks.stop()
     ms = t0.elapsed_time(t1) / K
     nbytes = 2 * rows * cols * 4 + rows * 4
@@ -707,7 +736,7 @@ def run_host(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE,

@@ -20,27 +20,31 @@
 // rings.  With causal masking only query blocks i with queries >= the block's
 // first key are visited.
 //
-// Every MMA has M = N = 128 (a 64-wide N runs at about half the tensor rate):
-// TMEM holds dK and dV (d columns each), a region X for S^T whose first half
-// is overwritten in place by the bf16 P^T, and a region Y that holds dP^T until
-// dS is formed and then dQ^T.  The MMA warp issues, per step i,
+// Every MMA has M = N = 128 (an SS MMA with a 64-wide N reads a full A operand
+// from shared memory for half the work): TMEM holds dK and dV (d columns each),
+// a region X for S^T whose first half is overwritten in place by the bf16 P^T,
+// and a region Y that holds dP^T, then (over dP^T's first half) the bf16 dS^T
+// that dK takes as its TMEM operand, and then dQ^T.  The MMA warp issues, per
+// step i,
 //
 //   dP(i) -> Y  dV(i)  S(i+1) -> X  dK(i) (first half)  dK(i) (second half)  dQ(i) -> Y
 //
 // dP(i) does not wait for P(i), so dS(i) starts as soon as it lands; dV(i) and
 // S(i+1) execute while dS(i) is formed, and so does the half of dK(i) over the
 // queries of the compute warps' first pass.  P(i+1) is formed while the rest
-// of dK(i), dQ(i) and the next dP execute.  Each compute warpgroup keeps the bf16 P^T
-// of its 64 queries in registers from P to dS, so X can take S(i+1) right
-// after dV(i).  The dQ^T partial of each
-// step is read out of TMEM by a drain warpgroup (freeing Y for dP(i+1)) and
+// of dK(i), dQ(i) and the next dP execute.  Each compute warpgroup keeps the
+// bf16 P^T of its 64 queries in registers from P to dS, so X can take S(i+1)
+// right after dV(i).  The dQ^T partial of each step is read out of TMEM by a
+// drain warpgroup (freeing Y for dP(i+1)) and
 // added into an fp32 accumulator with bulk tensor reduces of 16 query rows,
 // staged round-robin through four shared-memory buffers so that filling one
 // overlaps the reduces reading the others (two buffers were 11 % faster than
 // one, three 1.2 % faster than two, four 3.8 % faster than three).  Each SM's
 // bulk-copy unit adds at most about 25 bytes per cycle, and a step hands it
-// 64 KB, so these reductions are what bounds the kernel.  The alternative, a second pass parallel over query blocks, would
-// recompute S and dP (seven matmuls per tile instead of five).
+// 64 KB; together with the MMA operands, TMA loads, dS stores and the staging
+// they share shared-memory bandwidth, and these two bound the kernel.  The
+// alternative, a second pass parallel over query blocks, would recompute S and
+// dP (seven matmuls per tile instead of five).
 //
 // Warp roles (512 threads): warps 0-7 form P and dS, warpgroup w for queries
 // [64w, 64w + 64) of each step (thread t of a warpgroup owns key row t = TMEM

@@ -108,7 +108,10 @@ size_t fattn_bwd_workspace_bytes(int B, int H, int N, int d);
  * nothing launched.  NULL -> the call takes the scratch from the CUDA
  * stream-ordered allocator: cudaMallocAsync on `stream` before its kernels and
  * cudaFreeAsync on `stream` after them (workspace_bytes is then ignored); an
- * allocation failure returns FATTN_ERR_CUDA and launches nothing. */
+ * allocation failure returns FATTN_ERR_CUDA and launches nothing.  The
+ * device's default memory pool keeps nothing across synchronisations unless
+ * its release threshold is raised, so a program that calls this repeatedly
+ * saves a fresh mapping of the scratch each time by passing a workspace. */
 int fattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
               const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
               float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);

@@ -110,8 +110,8 @@ size_t fattn_bwd_workspace_bytes(int B, int H, int N, int d);
  * cudaFreeAsync on `stream` after them (workspace_bytes is then ignored); an
  * allocation failure returns FATTN_ERR_CUDA and launches nothing.  The
  * device's default memory pool keeps nothing across synchronisations unless
- * its release threshold is raised, so a program that calls this repeatedly
- * saves a fresh mapping of the scratch each time by passing a workspace. */
+ * its release threshold is raised, so each such call maps its scratch anew;
+ * a program that calls this repeatedly avoids that by passing a workspace. */
 int fattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
               const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
               float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);

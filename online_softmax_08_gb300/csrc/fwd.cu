@@ -1,7 +1,8 @@
 // fwd.cu -- FlashAttention forward for sm_103a (tcgen05 + TMEM + TMA).
 //
 // One CTA owns 256 query rows of one (batch, head): two 128-row subtiles
-// Q_0, Q_1, each running the single-query recurrence of "tm_flash_attention_math"
+// Q_0, Q_1 (SUB = 2; at d = 64 a CTA may own one, see below), each running
+// the single-query recurrence of "tm_flash_attention_math"
 // ("The block-wise update, and the full algorithm") for all of its rows at
 // once.  K/V tiles of 128 keys stream through a ring of shared-memory slots
 // filled by TMA; the score tile S = Q K^T lives only in TMEM ("A score tile is
@@ -33,6 +34,13 @@
 // half while the softmax forms the second; per subtile it issues all of
 // O_s += P_s V_j before S_s = Q_s K_{j+1}^T (the pipe runs them in order).
 // Shared memory: Q_0, Q_1 | K/V ring.
+//
+// SUB = 1 (d = 64 only): one 128-row subtile per CTA, 256 threads (softmax
+// warps 0-3, MMA warp 4, TMA warp 5, warps 6-7 idle), 256 TMEM columns (S, O,
+// P) and a 5-slot ring, so that two CTAs share an SM.  Their barrier chains
+// then run independently, and a short grid's last wave is split finer.  Each
+// CTA streams its own K/V, twice the L2 traffic of SUB = 2, so the launcher
+// takes it only for grids of a few waves.
 // setmaxnreg regions may not call functions: inline the wait's slow path
 #define FATTN_INLINE_WAIT_SLOW_PATH
 #include "common.cuh"
@@ -85,31 +93,42 @@ __device__ __forceinline__ void add_x2(float& s0, float& s1, float a0, float a1)
       : "f"(a0), "f"(a1));
 }
 
-template <int D>
+template <int D, int SUB_>
 struct Fwd {
+  static constexpr int SUB = SUB_;                // 128-row Q subtiles per CTA
+  static_assert(SUB == 2 || (SUB == 1 && D == 64), "one subtile per CTA at d = 64 only");
+  static constexpr int ROWS = 128 * SUB;          // query rows per CTA
+  static constexpr int MIN_CTAS = SUB == 1 ? 2 : 1;  // CTAs sharing an SM
   static constexpr int BM = 128;                  // rows per Q subtile
   static constexpr int BN = 128;                  // keys per K/V tile
   static constexpr int HALF = BM * 128;           // one 64-column, 128-row swizzled half (bytes)
   static constexpr int TILE = BM * D * 2;         // Q, K, V or O tile (bf16)
-  static constexpr int STAGES = D == 128 ? 5 : 8; // K/V ring slots
+  static constexpr int STAGES = D == 128 ? 5 : (SUB == 1 ? 5 : 8);  // K/V ring slots
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = OFF_Q + 2 * TILE;
+  static constexpr int OFF_KV = OFF_Q + SUB * TILE;
   static constexpr int OFF_BAR = OFF_KV + STAGES * TILE;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers + alignment slack
-  static constexpr int THREADS = 384;  // three warpgroups (warps 10, 11 idle)
+  // SUB softmax warpgroups and one control warpgroup (MMA warp, TMA warp, two idle)
+  static constexpr int THREADS = 128 * (SUB + 1);
+  static constexpr int W_MMA = 4 * SUB, W_TMA = 4 * SUB + 1;
   // registers per thread after setmaxnreg; the launch holds THREADS x REG_LAUNCH
-  static constexpr int REG_LAUNCH = 168, REG_SOFTMAX = 224, REG_CTRL = 48;
-  static_assert((2 * REG_SOFTMAX + REG_CTRL) * 128 <= THREADS * REG_LAUNCH, "register split");
+  static constexpr int REG_LAUNCH = SUB == 1 ? 128 : 168;
+  static constexpr int REG_SOFTMAX = SUB == 1 ? 208 : 224, REG_CTRL = 48;
+  static_assert((SUB * REG_SOFTMAX + REG_CTRL) * 128 <= THREADS * REG_LAUNCH, "register split");
+  static_assert(MIN_CTAS * (SMEM + 1024) <= 233472, "shared memory of the CTAs sharing an SM");
+  // the registers admit at most MIN_CTAS CTAs per SM, so their TMEM allocations never wait
+  static_assert((MIN_CTAS + 1) * THREADS * REG_LAUNCH > 65536, "a third CTA would wait for TMEM");
+  static constexpr int TMEM_COLS = SUB == 1 ? 256 : 512;
   static constexpr uint32_t TM_S = 0;
-  static constexpr uint32_t TM_O = 256;
+  static constexpr uint32_t TM_O = 128 * SUB;
   // d = 64 leaves 128 TMEM columns free: P_s gets a region of its own there
   // (64 columns of bf16 pairs per subtile), so S_s = Q_s K_{j+1}^T can be
   // issued as soon as the softmax has read S_s(j) into registers, instead of
   // after O_s += P_s V_j; the softmax then never waits on its own subtile's MMAs
   static constexpr bool DEC = D == 64 && FATTN_FWD_DEC64 != 0;
-  static constexpr uint32_t TM_P = DEC ? TM_O + 2 * D : TM_S;  // P_s at TM_P + (DEC ? 64 : 128) s
+  static constexpr uint32_t TM_P = DEC ? TM_O + SUB * D : TM_S;  // P_s at TM_P + (DEC ? 64 : 128) s
   static constexpr uint32_t P_STRIDE = DEC ? 64 : 128;
-  static_assert(!DEC || TM_P + 2 * 64 <= 512, "TMEM budget");
+  static_assert(!DEC || TM_P + SUB * 64 <= TMEM_COLS, "TMEM budget");
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
 };
@@ -126,20 +145,21 @@ enum {
   B_KV_FULL = 12,  // [STAGES], then kv_empty [STAGES]
 };
 // the barriers, the TMEM address slot and the abort flag share 256 bytes
-static_assert(8 * (B_KV_FULL + 2 * Fwd<64>::STAGES) + 8 <= 256, "barrier block");
-static_assert(8 * (B_KV_FULL + 2 * Fwd<128>::STAGES) + 8 <= 256, "barrier block");
+static_assert(8 * (B_KV_FULL + 2 * Fwd<64, 2>::STAGES) + 8 <= 256, "barrier block");
+static_assert(8 * (B_KV_FULL + 2 * Fwd<64, 1>::STAGES) + 8 <= 256, "barrier block");
+static_assert(8 * (B_KV_FULL + 2 * Fwd<128, 2>::STAGES) + 8 <= 256, "barrier block");
 
 // VARLEN: the CTA's sequence comes from p.vl.cu_seqlens (packed head-major
 // rows); otherwise the dense [B, H, N, d] layout.  SPLIT (dense only): the CTA
 // covers one range of key tiles and writes its normalised partial O and LSE
 // (fp32) for the merge kernel; queries are the last p.Nq positions.
-template <int D, bool VARLEN, bool SPLIT>
-__global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
+template <int D, int SUB, bool VARLEN, bool SPLIT>
+__global__ void __launch_bounds__(Fwd<D, SUB>::THREADS, Fwd<D, SUB>::MIN_CTAS)
     fattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
-  using C = Fwd<D>;
+  using C = Fwd<D, SUB>;
   constexpr int ST = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -150,7 +170,7 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
   // SPLIT: blockIdx = (query block, unit, split) with the split fastest
   const int split = SPLIT ? (int)(blockIdx.x % (unsigned)p.n_splits) : 0;
   const unsigned bidx = SPLIT ? blockIdx.x / (unsigned)p.n_splits : blockIdx.x;
-  const int n_qb = ((SPLIT ? p.Nq : p.N) + 255) / 256;  // p.N: the (longest) sequence length
+  const int n_qb = ((SPLIT ? p.Nq : p.N) + C::ROWS - 1) / C::ROWS;  // p.N: the (longest) sequence length
   // heaviest (last) query blocks first
   // dense: query-block-major within groups of heads; varlen:
   // one (sequence, head) unit after another, so the CTAs in flight share their
@@ -171,7 +191,7 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
       if (threadIdx.x == 0 && p.err) atomicCAS(p.err, 0u, (unsigned)(ERR_SITE_FWD | 0x40));
       return;
     }
-    if (qb * 256 >= seq.N) return;  // this sequence is shorter: nothing to do
+    if (qb * C::ROWS >= seq.N) return;  // this sequence is shorter: nothing to do
   } else {
     seq = SeqView{p.N, 0, unit, (long long)unit * p.N};
   }
@@ -191,7 +211,8 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
     const int last_key = p.causal ? min(r0 + C::BM - 1 + off, N - 1) : N - 1;
     return max(0, min(last_key / C::BN + 1, jhi) - jlo);
   };
-  const int r0_0 = qb * 256, r0_1 = qb * 256 + 128;
+  // with one subtile, subtile 1 starts past every sequence and sees no tiles
+  const int r0_0 = qb * C::ROWS, r0_1 = SUB == 2 ? r0_0 + 128 : (1 << 30);
   const int nt0 = tiles_for(r0_0), nt1 = tiles_for(r0_1);
   const int r0[2] = {r0_0, r0_1};
   const int nt[2] = {nt0, nt1};
@@ -222,7 +243,7 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -230,9 +251,9 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 10) {
+  if (warp > C::W_TMA) {
     regs_dec<C::REG_CTRL>();  // idle
-  } else if (warp == 9) {
+  } else if (warp == C::W_TMA) {
     regs_dec<C::REG_CTRL>();
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
@@ -269,7 +290,7 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
       mbar_drain(bar(B_Q), 0, wctx, ERR_SITE_FWD | 0x03);
     }
     __syncwarp();
-  } else if (warp == 8) {
+  } else if (warp == C::W_MMA) {
     regs_dec<C::REG_CTRL>();
     // ---------------------------------------------------------------- MMA issuer (whole warp)
     {
@@ -602,36 +623,41 @@ __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
-template <int D, bool VARLEN, bool SPLIT>
+// Query blocks of ROWS rows the grid covers, times the units (and splits).
+template <int ROWS, bool VARLEN, bool SPLIT>
+long long fwd_blocks(const FwdParams& p) {
+  const long long n_qb = ((SPLIT ? p.Nq : p.N) + ROWS - 1) / ROWS;
+  return n_qb * (VARLEN ? (long long)p.vl.B * p.vl.H : p.BH) * (SPLIT ? p.n_splits : 1);
+}
+
+template <int D, int SUB, bool VARLEN, bool SPLIT>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                    const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
-  using C = Fwd<D>;
+  using C = Fwd<D, SUB>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
   static_assert(!(VARLEN && SPLIT), "split-KV is dense only");
   static unsigned long long prepared[64];
   cudaError_t e = prepare_once(prepared, [] {
-    cudaError_t r = cudaFuncSetAttribute(fattn_fwd_kernel<D, VARLEN, SPLIT>,
+    cudaError_t r = cudaFuncSetAttribute(fattn_fwd_kernel<D, SUB, VARLEN, SPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (r != cudaSuccess) return r;
     // the setmaxnreg split hands out at most the launch's registers; with fewer
     // at launch an increase would never be granted
     cudaFuncAttributes fa;
-    r = cudaFuncGetAttributes(&fa, fattn_fwd_kernel<D, VARLEN, SPLIT>);
+    r = cudaFuncGetAttributes(&fa, fattn_fwd_kernel<D, SUB, VARLEN, SPLIT>);
     if (r != cudaSuccess) return r;
     return fa.numRegs >= C::REG_LAUNCH ? cudaSuccess : cudaErrorInvalidConfiguration;
   });
   if (e != cudaSuccess) return e;
-  const long long n_qb = ((SPLIT ? p.Nq : p.N) + 255) / 256;
-  const long long blocks = n_qb * (VARLEN ? (long long)p.vl.B * p.vl.H : p.BH) *
-                           (SPLIT ? p.n_splits : 1);
+  const long long blocks = fwd_blocks<C::ROWS, VARLEN, SPLIT>(p);
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (blocks == 0) return cudaSuccess;
-  fattn_fwd_kernel<D, VARLEN, SPLIT><<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv,
-                                                                                        to, p);
+  fattn_fwd_kernel<D, SUB, VARLEN, SPLIT><<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(
+      tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
@@ -640,18 +666,30 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
   const bool vl = p.vl.cu_seqlens != nullptr;
-  if (d == 128) return vl ? launch<128, true, false>(tq, tk, tv, to, p, stream)
-                          : launch<128, false, false>(tq, tk, tv, to, p, stream);
-  if (d == 64) return vl ? launch<64, true, false>(tq, tk, tv, to, p, stream)
-                         : launch<64, false, false>(tq, tk, tv, to, p, stream);
+  if (d == 128) return vl ? launch<128, 2, true, false>(tq, tk, tv, to, p, stream)
+                          : launch<128, 2, false, false>(tq, tk, tv, to, p, stream);
+  if (d == 64) {
+    // One subtile per CTA (two CTAs per SM) when the two-subtile grid would be
+    // at most six waves.  Measured at B4 H16 N2048, B8 H16 N1024, B1 H16 N8192
+    // and B2 H16 N6144: 4-13 % faster without a mask, 0-6 % with the causal
+    // one; at 6.7 waves and more (B1 H16 N16384, B1 H64 N8192) the doubled K/V
+    // traffic from L2 made it 0-3 % slower.
+    const long long two = vl ? fwd_blocks<256, true, false>(p) : fwd_blocks<256, false, false>(p);
+    const int n_sm = device_sm_count();
+    if (n_sm > 0 && two <= 6LL * n_sm)
+      return vl ? launch<64, 1, true, false>(tq, tk, tv, to, p, stream)
+                : launch<64, 1, false, false>(tq, tk, tv, to, p, stream);
+    return vl ? launch<64, 2, true, false>(tq, tk, tv, to, p, stream)
+              : launch<64, 2, false, false>(tq, tk, tv, to, p, stream);
+  }
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_fwd_split(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                              const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& p,
                              cudaStream_t stream) {
-  if (d == 128) return launch<128, false, true>(tq, tk, tv, to, p, stream);
-  if (d == 64) return launch<64, false, true>(tq, tk, tv, to, p, stream);
+  if (d == 128) return launch<128, 2, false, true>(tq, tk, tv, to, p, stream);
+  if (d == 64) return launch<64, 2, false, true>(tq, tk, tv, to, p, stream);
   return cudaErrorInvalidValue;
 }
 

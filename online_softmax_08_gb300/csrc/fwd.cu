@@ -225,7 +225,22 @@ __global__ void __launch_bounds__(Fwd<D, SUB>::THREADS, Fwd<D, SUB>::MIN_CTAS)
   volatile uint32_t* abort_flag = tmem_slot + 1;
   const WaitCtx wctx{abort_flag, p.err};
 
-  if (threadIdx.x == 0) {
+  // The TMA thread initialises the barriers and issues Q and the first ST K/V
+  // loads (their slots are empty) before the CTA-wide sync, so that the load
+  // latency overlaps the TMEM allocation and the sync.
+  const bool tma_thread = warp == C::W_TMA && lane == 0;
+  const int n_loads = 2 * n_max;
+  const int n_pre = min(ST, n_loads);
+  auto load_kv = [&](int i) {
+    const int slot = i % ST;
+    const uint32_t dst = sbase + C::OFF_KV + slot * C::TILE;
+    const CUtensorMap* m = (i & 1) ? &tm_v : &tm_k;
+    mbar_arrive_expect_tx(kv_full0 + 8u * slot, C::TILE);
+    for (int h = 0; h < D / 64; ++h)
+      tma_load_3d(dst + h * C::HALF, m, kv_full0 + 8u * slot, h * 64,
+                  row0 + (jlo + (i >> 1)) * C::BN, bh);
+  };
+  if (tma_thread) {
     mbar_init(bar(B_Q), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_S_FULL + s), 1);
@@ -241,6 +256,18 @@ __global__ void __launch_bounds__(Fwd<D, SUB>::THREADS, Fwd<D, SUB>::MIN_CTAS)
     }
     *abort_flag = 0u;
     fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    const uint32_t q_bytes = (uint32_t)((nt0 > 0) + (nt1 > 0)) * C::TILE;
+    mbar_arrive_expect_tx(bar(B_Q), q_bytes);
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+      if (nt[s] > 0)
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(sbase + C::OFF_Q + s * C::TILE + h * C::HALF, &tm_q, bar(B_Q), h * 64,
+                      row0 + r0[s], bh);
+    for (int i = 0; i < n_pre; ++i) load_kv(i);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -257,31 +284,13 @@ __global__ void __launch_bounds__(Fwd<D, SUB>::THREADS, Fwd<D, SUB>::MIN_CTAS)
     regs_dec<C::REG_CTRL>();
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      const uint32_t q_bytes = (uint32_t)((nt0 > 0) + (nt1 > 0)) * C::TILE;
-      mbar_arrive_expect_tx(bar(B_Q), q_bytes);
-#pragma unroll
-      for (int s = 0; s < 2; ++s)
-        if (nt[s] > 0)
-          for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(sbase + C::OFF_Q + s * C::TILE + h * C::HALF, &tm_q, bar(B_Q), h * 64,
-                        row0 + r0[s], bh);
-      const int n_loads = 2 * n_max;
-      int issued = 0;
-      for (int i = 0; i < n_loads; ++i) {
+      int issued = n_pre;  // Q and loads [0, n_pre) went out before the sync
+      for (int i = n_pre; i < n_loads; ++i) {
         const int slot = i % ST, use = i / ST;
         // a slot is refilled only after the MMAs that read it completed; when
         // the CTA is aborting nothing more is issued
-        if (use > 0 && !mbar_wait(kv_empty0 + 8u * slot, (use - 1) & 1, wctx, ERR_SITE_FWD | 0x01))
-          break;
-        const uint32_t dst = sbase + C::OFF_KV + slot * C::TILE;
-        const CUtensorMap* m = (i & 1) ? &tm_v : &tm_k;
-        mbar_arrive_expect_tx(kv_full0 + 8u * slot, C::TILE);
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(dst + h * C::HALF, m, kv_full0 + 8u * slot, h * 64,
-                      row0 + (jlo + (i >> 1)) * C::BN, bh);
+        if (!mbar_wait(kv_empty0 + 8u * slot, (use - 1) & 1, wctx, ERR_SITE_FWD | 0x01)) break;
+        load_kv(i);
         issued = i + 1;
       }
       // drain: at most one load per slot can still be landing, the latest one
@@ -606,7 +615,7 @@ __global__ void __launch_bounds__(Fwd<D, SUB>::THREADS, Fwd<D, SUB>::MIN_CTAS)
           for (int h = 0; h < D / 64; ++h)
             tma_store_3d(&tm_o, o_base + h * C::HALF, h * 64, row0 + my_r0, bh);
           bulk_commit();
-          bulk_wait_all();
+          bulk_wait_read_all();  // the CTA's exit needs only the shared-memory reads done
         }
       }
       if (row < N) p.lse[seq.stat0 + row] = (m_run * sl2 + lg2(l_run)) * kLn2;

@@ -236,7 +236,9 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
   volatile uint32_t* abort_flag = tmem_slot + 1;
   const WaitCtx wctx{abort_flag, p.err};
 
-  if (threadIdx.x == 0) {
+  // The loader thread initialises the barriers and issues the K and V loads
+  // before the CTA-wide sync, so their latency overlaps the TMEM allocation.
+  if (warp == 13 && lane == 0) {
     mbar_init(bar(B_KV), 1);
     mbar_init(bar(B_S_FULL), 1);
     mbar_init(bar(B_P_FULL), 256);
@@ -257,6 +259,13 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
     }
     *abort_flag = 0u;
     fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_do);
+    mbar_arrive_expect_tx(bar(B_KV), 2 * C::TILE);
+    for (int h = 0; h < D / 64; ++h) {
+      tma_load_3d(sbase + C::OFF_K + h * C::HALF, &tm_k, bar(B_KV), h * 64, row0 + k0, bh);
+      tma_load_3d(sbase + C::OFF_V + h * C::HALF, &tm_v, bar(B_KV), h * 64, row0 + k0, bh);
+    }
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -271,15 +280,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
     regs_dec<C::REG_CTRL>();
     if (warp == 13) {
       // ---------------------------------------------------------------- loads
-      if (lane == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_do);
-        mbar_arrive_expect_tx(bar(B_KV), 2 * C::TILE);
-        for (int h = 0; h < D / 64; ++h) {
-          tma_load_3d(sbase + C::OFF_K + h * C::HALF, &tm_k, bar(B_KV), h * 64, row0 + k0, bh);
-          tma_load_3d(sbase + C::OFF_V + h * C::HALF, &tm_v, bar(B_KV), h * 64, row0 + k0, bh);
-        }
-      }
+      // (K and V went out before the sync)
       const float kLog2e = 1.4426950408889634f;
       int q_issued = 0, o_issued = 0;
       // Q(i) is released by dK(i), dO(i) by dV(i); in the MMA order dV(i) precedes
@@ -481,7 +482,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
         }
       }
     }
-    if (t == 0) bulk_wait_all();
+    if (t == 0) bulk_wait_read_all();  // the CTA's exit needs only the shared-memory reads done
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- compute (warps 0-7)
@@ -663,7 +664,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
           tma_store_3d(&tm_dv, sbase + C::OFF_V + h * C::HALF, h * 64, row0 + k0, bh);
         }
         bulk_commit();
-        bulk_wait_all();
+        bulk_wait_read_all();
       }
     }
     __syncwarp();

@@ -169,6 +169,31 @@ def test_b4h16_n2048_d64_all_heads(causal):
     _all_heads("b4h16_n2048_d64", causal, heads_per_call=16)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_d64_grid_of_two_subtile_ctas(causal):
+    """At d = 64 the launcher gives each CTA one 128-row subtile (two CTAs per
+    SM) while the two-subtile grid would be at most six waves, and two subtiles
+    per CTA beyond that.  C2 and the small cases take the first form; this
+    shape, sized from the device's SM count, takes the second.  Four heads are
+    compared element by element, and the tile counts of all of them."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    N, d = 2048, 64
+    H = 16
+    B = -(-(6 * n_sm + 1) // (H * (N // 256)))  # two-subtile CTAs > 6 waves
+    assert B * H * (N // 256) > 6 * n_sm
+    q, k, v = make_inputs(B, H, N, d, seed=4242, q_std=1.0, v_dist="normal")
+    scale = default_scale(d)
+    o, lse, counts = _run(q, k, v, scale, causal, counts=True)
+    assert counts == _expected_counts(B, H, N, d, causal)
+    qf, kf, vf = _f64(q), _f64(k), _f64(v)
+    o, lse = _f64(o).reshape(B * H, N, d), _f64(lse).reshape(B * H, N)
+    heads = [0, 1, (B * H) // 2, B * H - 1]
+    sl = lambda x: np.ascontiguousarray(x.reshape(B * H, N, -1)[heads][None])
+    o_ref, lse_ref = oracle.attention_fwd(sl(qf), sl(kf), sl(vf), scale, causal)
+    _check(o[heads], lse[heads], o_ref[0], lse_ref[0],
+           case="B%d H%d N%d d64 %s fwd (two-subtile grid), 4 heads" % (B, H, N, "causal" if causal else "non-causal"))
+
+
 def test_headline_b1h32_n8192_d128_causal_all_heads():
     _all_heads("b1h32_n8192_d128_causal", True)
 

@@ -63,6 +63,18 @@ def test_varlen_forward_and_backward_match_oracle(lengths, H, d, causal):
         _close(_f64(got), want)
 
 
+def test_varlen_d64_grid_of_two_subtile_ctas():
+    """The d = 64 varlen forward on a grid large enough (from the device's SM
+    count) for two 128-row subtiles per CTA, forward and backward against the
+    oracle on every sequence."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    H, d = 8, 64
+    n_seq = -(-(6 * n_sm + 1) // (H * 8))  # 8 blocks of 256 rows for the longest sequence
+    lengths = [2048] + [(97 * i) % 1500 + 1 for i in range(1, n_seq)]
+    assert n_seq * H * 8 > 6 * n_sm
+    test_varlen_forward_and_backward_match_oracle(lengths, H, d, True)
+
+
 def test_varlen_with_equal_lengths_equals_the_dense_kernels():
     """The packed path on B equal-length sequences gives the dense path's bits
     for O and LSE (the same tiles, masks and order) and the same gradients to

@@ -237,9 +237,10 @@ int launch_bwd_all(const void* q, const void* k, const void* v, const void* o, c
       !make_bf16_map(&tk, k, d, R, Z, bk) || !make_bf16_map(&tv, v, d, R, Z, bk) ||
       !make_bf16_map(&tdk, dk, d, R, Z, bk) || !make_bf16_map(&tdv, dv, d, R, Z, bk))
     return FATTN_ERR_CUDA;
-  // dQ accumulator: fp32, add-reduced bwd_dq_rows() query rows at a time
-  if (!make_map(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, R, Z, d, bwd_dq_rows(),
-                CU_TENSOR_MAP_SWIZZLE_NONE))
+  // dQ accumulator: fp32, add-reduced one box of query rows at a time
+  const DqBox qb = bwd_dq_box(d);
+  if (!make_map(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, R, Z, qb.cols, qb.rows,
+                qb.sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE))
     return FATTN_ERR_CUDA;
   auto mark = [&](int i) {
     return !phase_events ||

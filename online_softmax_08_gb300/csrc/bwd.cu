@@ -20,35 +20,46 @@
 // rings.  With causal masking only query blocks i with queries >= the block's
 // first key are visited.
 //
-// Every MMA has M = N = 128 (an SS MMA with a 64-wide N reads a full A operand
-// from shared memory for half the work): TMEM holds dK and dV (d columns each),
-// a region X for S^T whose first half is overwritten in place by the bf16 P^T,
-// and a region Y that holds dP^T, then (over dP^T's first half) the bf16 dS^T
-// that dK takes as its TMEM operand, and then dQ^T.  The MMA warp issues, per
-// step i,
+// Every MMA has M = 128 and, but for dQ at d = 64, N = 128 (an SS MMA with a
+// 64-wide N reads a full A operand from shared memory for half the work):
+// TMEM holds dK and dV (d columns each), a region X for S^T whose first half is
+// overwritten in place by the bf16 P^T, and a region Y that holds dP^T, then
+// (over dP^T's first half) the bf16 dS^T that dK takes as its TMEM operand.
+// The MMA warp issues, per step i,
 //
-//   dP(i) -> Y  dV(i)  S(i+1) -> X  dK(i) (first half)  dK(i) (second half)  dQ(i) -> Y
+//   dP(i) -> Y  dV(i)  S(i+1) -> X  dK(i) (first half)  dK(i) (second half)  dQ(i)
 //
 // dP(i) does not wait for P(i), so dS(i) starts as soon as it lands; dV(i) and
 // S(i+1) execute while dS(i) is formed, and so does the half of dK(i) over the
 // queries of the compute warps' first pass.  P(i+1) is formed while the rest
 // of dK(i), dQ(i) and the next dP execute.  Each compute warpgroup keeps the
 // bf16 P^T of its 64 queries in registers from P to dS, so X can take S(i+1)
-// right after dV(i).  The dQ^T partial of each step is read out of TMEM by a
-// drain warpgroup (freeing Y for dP(i+1)) and
-// added into an fp32 accumulator with bulk tensor reduces of 16 query rows,
-// staged round-robin through four shared-memory buffers so that filling one
-// overlaps the reduces reading the others (two buffers were 11 % faster than
-// one, three 1.2 % faster than two, four 3.8 % faster than three).  Each SM's
-// bulk-copy unit adds at most about 25 bytes per cycle, and a step hands it
-// 64 KB; together with the MMA operands, TMA loads, dS stores and the staging
-// they share shared-memory bandwidth, and these two bound the kernel.  The
-// alternative, a second pass parallel over query blocks, would recompute S and
-// dP (seven matmuls per tile instead of five).
+// right after dV(i).  The MMA pipe runs in issue order, so dP(i + 1)'s commit
+// also tells the compute warps that dK(i) and dQ(i) have read dS^T(i).
+//
+// d = 128: dQ^T = K^T dS^T (M = d) goes over dP^T in Y.  A drain warpgroup reads
+// it out of TMEM (freeing Y for dP(i+1)) and adds it into an fp32 accumulator
+// with bulk tensor reduces of 16 query rows, staged round-robin through four
+// shared-memory buffers so that filling one overlaps the reduces reading the
+// others (two buffers were 11 % faster than one, three 1.2 % faster than two,
+// four 3.8 % faster than three).  Each SM's bulk-copy unit adds at most about
+// 25 bytes per cycle, and a step hands it 64 KB; together with the MMA
+// operands, TMA loads, dS stores and the staging they share shared-memory
+// bandwidth, and these two bound the kernel.
+//
+// d = 64: dQ^T would be an M = 128 MMA half of which is padding, so dQ = dS K
+// (M = 128 queries, N = 64) is computed instead, into a TMEM region Z of its
+// own: only the next dQ waits for the drain.  Each drain warp holds 32 query
+// rows and adds them by itself, with reduces of 32 rows x 32 columns through
+// two buffers of its own (16 % faster than dQ^T over Y for the whole non-causal
+// backward at B 4, H 16, N 2048, 12 % causal).
+//
+// The alternative to the dQ reduces, a second pass parallel over query blocks,
+// would recompute S and dP (seven matmuls per tile instead of five).
 //
 // Warp roles (512 threads): warps 0-7 form P and dS, warpgroup w for queries
 // [64w, 64w + 64) of each step (thread t of a warpgroup owns key row t = TMEM
-// lane t), warps 8-11 drain dQ, warp 12 issues MMAs (the whole warp runs the
+// lane t), warps 8-11 drain dQ (or dQ^T), warp 12 issues MMAs (the whole warp runs the
 // loop, elect.sync picks the issuing lane), warp 13 issues TMA loads and stages
 // LSE and D, warps 14-15 idle.  Registers move from the last warpgroup to the
 // drain warpgroup (setmaxnreg).
@@ -91,17 +102,29 @@ struct Bwd {
   // NDQ - 1 bulk reduces are in flight while the next buffer is filled
   static constexpr int RPC = FATTN_DQ_ROWS;
   static constexpr int NDQ = FATTN_DQ_BUFS;
-  static constexpr int CPS = BQ / RPC;  // chunks per step
-  static constexpr int OFF_DQ = OFF_STAT + QST * 2 * BQ * 4;  // fp32 staging [NDQ][RPC q][D]
-  static constexpr int OFF_BAR = OFF_DQ + NDQ * RPC * D * 4;
+  // at d = 64 dQ = dS K is an N = 64 MMA with queries on the TMEM lanes (dQ^T would
+  // need M = 128, half of it padding): each drain warp adds its own 32 query rows
+  // with reduces of 32 rows x 32 columns (128-byte swizzled), through two buffers
+  // of its own
+  static constexpr bool DQ_QL = D == 64;
+  static constexpr int DQ_WBUF = 32 * D * 4;  // one drain warp's 32 rows (fp32)
+  static constexpr int OFF_DQ = OFF_STAT + QST * 2 * BQ * 4;  // fp32 staging
+  static constexpr int DQ_BYTES = DQ_QL ? 4 * 2 * DQ_WBUF : NDQ * RPC * D * 4;
+  static constexpr int OFF_BAR = OFF_DQ + DQ_BYTES;
   static constexpr int SLACK = FATTN_SMEM_SLACK;
   static constexpr int SMEM = OFF_BAR + 256 + SLACK;
   static constexpr int THREADS = 512;
   static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_X = 2 * D, TM_Y = 2 * D + 128;
+  // where dQ (or dQ^T) goes: d = 64, a region Z of its own, so dP(i + 1) need not
+  // wait for the drain to read dQ(i); d = 128, over dP^T in Y (TMEM is full)
+  static constexpr bool DQ_OWN = 2 * D + 384 <= 512;
+  static constexpr uint32_t TM_Z = DQ_OWN ? 2 * D + 256 : TM_Y;
+  static_assert(!DQ_QL || DQ_OWN, "dQ with queries on the lanes needs its own region");
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BQ, false, false);   // S^T, dP^T
   static constexpr uint32_t IDESC_ACC = idesc_bf16_f32(128, D, false, true);   // dV, dK
-  // dQ^T = K^T dS^T with M = 128: at d = 64 the upper 64 rows are padding
-  static constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, BQ, true, true);
+  // d = 64: dQ = dS K (M = 128 queries, N = 64); d = 128: dQ^T = K^T dS^T
+  static constexpr uint32_t IDESC_DQ =
+      DQ_QL ? idesc_bf16_f32(BQ, D, true, true) : idesc_bf16_f32(128, BQ, true, true);
   // registers per thread after the split (sum x 128 threads = the launch's 65536)
   static constexpr int REG_COMPUTE = 128, REG_DRAIN = 200, REG_CTRL = 56;
   static_assert(2 * REG_COMPUTE + REG_DRAIN + REG_CTRL == 4 * 128, "register split");
@@ -127,15 +150,14 @@ enum {
   B_DS_HALF = 3,    // compute warps -> MMA: the first 32 queries of each half of dS^T in TMEM
   B_DP_FULL = 4,    // MMA -> compute warps: dP^T in Y
   B_DS_FULL = 5,    // compute warps -> MMA: dS^T in TMEM and shared memory, dP^T read
-  B_DS_FREE = 6,    // MMA -> compute warps: dK and dQ have read dS^T
-  B_DQ_FULL = 7,    // MMA -> drain: dQ^T in Y
-  B_DQ_FREE = 8,    // drain -> MMA: dQ^T read, Y may be overwritten
-  B_MMA_DONE = 9,   // MMA -> epilogue and the MMA warp's drain: every MMA finished
-  B_Q_FULL = 10,    // [QST] Q tile + LSE2, D of a step
-  B_Q_EMPTY = 13,   // [QST]
-  B_O_FULL = 16,    // [OST] dO tile
-  B_O_EMPTY = 18,   // [OST]
-  B_COUNT = 20,
+  B_DQ_FULL = 6,    // MMA -> drain: dQ (d = 64, in Z) or dQ^T (d = 128, in Y)
+  B_DQ_FREE = 7,    // drain -> MMA: dQ read, its region may be overwritten
+  B_MMA_DONE = 8,   // MMA -> epilogue and the MMA warp's drain: every MMA finished
+  B_Q_FULL = 9,     // [QST] Q tile + LSE2, D of a step
+  B_Q_EMPTY = 12,   // [QST]
+  B_O_FULL = 15,    // [OST] dO tile
+  B_O_EMPTY = 17,   // [OST]
+  B_COUNT = 19,
 };
 static_assert(Bwd<128>::QST <= 3 && Bwd<64>::QST <= 3 && Bwd<64>::OST <= 2, "barrier slots");
 
@@ -245,7 +267,6 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
     mbar_init(bar(B_DP_FULL), 1);
     mbar_init(bar(B_DS_HALF), 256);
     mbar_init(bar(B_DS_FULL), 256);
-    mbar_init(bar(B_DS_FREE), 1);
     mbar_init(bar(B_DQ_FULL), 1);
     mbar_init(bar(B_DQ_FREE), 128);
     mbar_init(bar(B_MMA_DONE), 1);
@@ -372,14 +393,16 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
                         (acc || kk > 0));
         }
       };
-      // dQ^T[128 x BQ] = K^T[d x keys] * dS^T[keys x BQ], both MN-major; at d = 64 the
-      // second 64-row block of A is read from the next tile (V) and is padding
+      // d = 64: dQ[BQ x D] = dS[BQ x keys] * K[keys x D]; d = 128: dQ^T[D x BQ] =
+      // K^T[D x keys] * dS^T[keys x BQ]; all operands MN-major
       auto mma_dq = [&]() {
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk) {
           const uint32_t o = kk * 16 * 128;
-          mma_bf16_ss_w(tmem + C::TM_Y, sdesc_sw128(sK + o, C::HALF, 1024),
-                        sdesc_sw128(sDS + o, C::HALF, 1024), C::IDESC_DQ, kk > 0);
+          const uint64_t dk_ = sdesc_sw128(sK + o, C::HALF, 1024);
+          const uint64_t ds_ = sdesc_sw128(sDS + o, C::HALF, 1024);
+          mma_bf16_ss_w(tmem + C::TM_Z, C::DQ_QL ? ds_ : dk_, C::DQ_QL ? dk_ : ds_, C::IDESC_DQ,
+                        kk > 0);
         }
       };
       auto wait_all = [&](int b, int parity, uint32_t site) {
@@ -397,10 +420,10 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
       }
       for (int it = 0; ok && it < n_it; ++it) {
         const bool next = it + 1 < n_it;
-        // dP(i) into Y once the drain has read dQ(i - 1): it does not wait for P(i),
-        // so dS(i) can start as soon as it lands
+        // dP(i) into Y (d = 128: once the drain has read dQ^T(i - 1) there): it does
+        // not wait for P(i), so dS(i) can start as soon as it lands
         if (!(ok = wait_all(B_O_FULL + it % OST, it / OST, 0x14))) break;
-        if (it > 0 && !(ok = wait_all(B_DQ_FREE, it - 1, 0x17))) break;
+        if (!C::DQ_OWN && it > 0 && !(ok = wait_all(B_DQ_FREE, it - 1, 0x17))) break;
         tc_fence_after();
         mma_xyT(C::TM_Y, sV, sDO(it));
         mma_commit_w(bar(B_DP_FULL));
@@ -425,9 +448,12 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
         tc_fence_after();
         mma_dk(sQ(it), true, 1);
         mma_commit_w(bar(B_Q_EMPTY + it % QST));  // dK is the last reader of Q(i)
+        if (C::DQ_OWN && it > 0) {  // Z: the drain has read dQ(i - 1)
+          if (!(ok = wait_all(B_DQ_FREE, it - 1, 0x17))) break;
+          tc_fence_after();
+        }
         mma_dq();
         mma_commit_w(bar(B_DQ_FULL));
-        mma_commit_w(bar(B_DS_FREE));
       }
       // drain: every MMA issued by this warp has finished before TMEM is freed
       mma_commit_w(bar(B_MMA_DONE));
@@ -440,50 +466,89 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
     const int t = threadIdx.x & 127;  // TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t sdq = sbase + C::OFF_DQ;
-    int nbuf = 0;  // chunks staged so far: the buffer of the next one is nbuf % NDQ
-    for (int it = 0; it < n_it; ++it) {
-      const int q0 = (i_start + it) * BQ;
-      mbar_wait(bar(B_DQ_FULL), it & 1, wctx, ERR_SITE_BWD | 0x31);
-      tc_fence_after();
-      uint32_t r[4][32];
+    if constexpr (C::DQ_QL) {
+      // thread t holds query row t of dQ (TMEM lane t, D columns); warp wd adds rows
+      // [32 wd, 32 wd + 32) on its own
+      const int wd = warp & 3;
+      for (int it = 0; it < n_it; ++it) {
+        const int q0 = (i_start + it) * BQ;
+        mbar_wait(bar(B_DQ_FULL), it & 1, wctx, ERR_SITE_BWD | 0x31);
+        tc_fence_after();
+        uint32_t r[D / 32][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + C::TM_Y + 32 * c, r[c]);
-      tmem_wait_ld();
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem + lane_off + C::TM_Z + 32 * c, r[c]);
+        tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) reg_fence32(r[c]);
-      tc_fence_before();
-      mbar_arrive(bar(B_DQ_FREE));
-      // lanes are d (lanes >= d are padding), columns are queries: stage 16 query
-      // rows at a time in shared memory and add them with one bulk tensor reduce
-      constexpr int RPC = C::RPC;
+        for (int c = 0; c < D / 32; ++c) reg_fence32(r[c]);
+        tc_fence_before();
+        mbar_arrive(bar(B_DQ_FREE));
+        const uint32_t buf = sdq + (uint32_t)((2 * wd + (it & 1)) * C::DQ_WBUF);
+        // this buffer's reduces, two steps ago, are done reading it
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
 #pragma unroll
-      for (int h = 0; h < C::CPS; ++h, ++nbuf) {  // RPC query rows per reduce
-        const uint32_t buf = sdq + (uint32_t)(nbuf % C::NDQ) * (RPC * D * 4);
-        // the reduce that last read this buffer, NDQ chunks ago, is done reading it
-        if (t == 0) bulk_wait_read<C::NDQ - 1>();
-        named_bar_sync(2, 128);
-        if (t < D) {
+        for (int c = 0; c < D / 32; ++c)  // 32 columns: one 128-byte-swizzled box
 #pragma unroll
-          for (int c = 0; c < RPC; ++c) {
-            const int q = h * RPC + c;  // query column of the dQ^T tile
-            asm volatile("st.shared.b32 [%0], %1;" ::"r"(buf + (uint32_t)(c * D + t) * 4u),
-                         "r"(r[q >> 5][q & 31])
-                         : "memory");
-          }
-        }
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(buf + c * 4096 + lane * 128 + ((j ^ (lane & 7)) << 4), r[c][4 * j],
+                         r[c][4 * j + 1], r[c][4 * j + 2], r[c][4 * j + 3]);
         fence_proxy_async_smem();
-        named_bar_sync(2, 128);
-        if (t == 0) {
+        __syncwarp();
+        if (lane == 0) {
           // rows past the sequence end belong to the next one (or lie past the
           // tensor, where TMA clips them): their partial is exactly zero, since
           // their LSE is +inf, so adding it changes nothing
-          tma_reduce_add_3d(&tm_dq, buf, 0, row0 + q0 + RPC * h, bh);
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c)
+            tma_reduce_add_3d(&tm_dq, buf + c * 4096, 32 * c, row0 + q0 + 32 * wd, bh);
           bulk_commit();
         }
       }
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+    } else {
+      int nbuf = 0;  // chunks staged so far: the buffer of the next one is nbuf % NDQ
+      for (int it = 0; it < n_it; ++it) {
+        const int q0 = (i_start + it) * BQ;
+        mbar_wait(bar(B_DQ_FULL), it & 1, wctx, ERR_SITE_BWD | 0x31);
+        tc_fence_after();
+        uint32_t r[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + C::TM_Z + 32 * c, r[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) reg_fence32(r[c]);
+        tc_fence_before();
+        mbar_arrive(bar(B_DQ_FREE));
+        // lanes are d (lanes >= d are padding), columns are queries: stage 16 query
+        // rows at a time in shared memory and add them with one bulk tensor reduce
+        constexpr int RPC = C::RPC, CPS = BQ / RPC;  // rows per reduce, reduces per step
+#pragma unroll
+        for (int h = 0; h < CPS; ++h, ++nbuf) {  // RPC query rows per reduce
+          const uint32_t buf = sdq + (uint32_t)(nbuf % C::NDQ) * (RPC * D * 4);
+          // the reduce that last read this buffer, NDQ chunks ago, is done reading it
+          if (t == 0) bulk_wait_read<C::NDQ - 1>();
+          named_bar_sync(2, 128);
+          if (t < D) {
+#pragma unroll
+            for (int c = 0; c < RPC; ++c) {
+              const int q = h * RPC + c;  // query column of the dQ^T tile
+              asm volatile("st.shared.b32 [%0], %1;" ::"r"(buf + (uint32_t)(c * D + t) * 4u),
+                           "r"(r[q >> 5][q & 31])
+                           : "memory");
+            }
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(2, 128);
+          if (t == 0) {  // (rows past the sequence end add zero, as above)
+            tma_reduce_add_3d(&tm_dq, buf, 0, row0 + q0 + RPC * h, bh);
+            bulk_commit();
+          }
+        }
+      }
+      if (t == 0) bulk_wait_read_all();  // the CTA's exit needs only the shared-memory reads done
+      __syncwarp();
     }
-    if (t == 0) bulk_wait_read_all();  // the CTA's exit needs only the shared-memory reads done
-    __syncwarp();
   } else {
     // ---------------------------------------------------------------- compute (warps 0-7)
     // Warpgroup w owns queries [64w, 64w + 64) of every step; thread t owns key
@@ -566,7 +631,6 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
       tmem_wait_ld();
       reg_fence32(u[0]);
       reg_fence32(u[1]);
-      if (it > 0) mbar_wait(bar(B_DS_FREE), (it - 1) & 1, wctx, ERR_SITE_BWD | 0x27);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         float ds[32];
@@ -684,7 +748,7 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
                    const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
   using C = Bwd<D>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
-  static_assert(C::TM_Y + 128 <= 512, "TMEM budget");
+  static_assert(C::TM_Y + 128 <= 512 && C::TM_Z + 128 <= 512, "TMEM budget");
   static unsigned long long prepared[64];
   cudaError_t e = prepare_once(prepared, [] {
     cudaError_t r = cudaFuncSetAttribute(fattn_bwd_kernel<D, VARLEN>,
@@ -709,7 +773,10 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
 
 }  // namespace
 
-int bwd_dq_rows() { return FATTN_DQ_ROWS; }
+DqBox bwd_dq_box(int d) {
+  if (Bwd<64>::DQ_QL && d == 64) return DqBox{32, 32, true};
+  return DqBox{d, FATTN_DQ_ROWS, false};
+}
 
 cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,

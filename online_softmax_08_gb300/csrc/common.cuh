@@ -161,7 +161,12 @@ cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tdq_acc, const BwdParams& p, cudaStream_t stream);
 // Query rows per bulk reduce of the backward's dQ partials (the box height of
 // the accumulator's tensor map).
-int bwd_dq_rows();
+// box of the dQ accumulator's bulk reduces: columns x query rows, 128-byte swizzle or none
+struct DqBox {
+  int cols, rows;
+  bool sw128;
+};
+DqBox bwd_dq_box(int d);
 cudaError_t launch_bwd_convert(const float* dq_acc, void* dq, long long n, float scale,
                                int n_sm, cudaStream_t stream);
 

@@ -126,7 +126,9 @@ struct Bwd {
   static constexpr uint32_t IDESC_DQ =
       DQ_QL ? idesc_bf16_f32(BQ, D, true, true) : idesc_bf16_f32(128, BQ, true, true);
   // registers per thread after the split (sum x 128 threads = the launch's 65536)
-  static constexpr int REG_COMPUTE = 128, REG_DRAIN = 200, REG_CTRL = 56;
+  // (64 for the MMA and loader warps: at 56 the MMA warp spilled, and its local
+  // loads sat in the issue loop that feeds the tensor pipe)
+  static constexpr int REG_COMPUTE = 128, REG_DRAIN = 192, REG_CTRL = 64;
   static_assert(2 * REG_COMPUTE + REG_DRAIN + REG_CTRL == 4 * 128, "register split");
   // TMEM column of the packed P^T for dV's K-step kk (16 queries = 8 columns); the
   // warpgroup of queries [64w, 64w + 64) keeps its P^T at X + 64w
@@ -143,21 +145,27 @@ struct Bwd {
 // Every barrier is waited on by parity, so no waiter may fall two phases
 // behind: each one below can only complete its next phase after its waiters
 // have consumed the current one (the MMA warp's issue order chains them).
+//
+// S_FULL has one slot per Q stage: the phase of step j's slot completes with the
+// loader's 32 arrivals (LSE2 and D of step j stored) and the commit of S(j).  The
+// loader arrives for step j + QST only after Q_EMPTY(j), which the compute warps
+// reach after their wait on step j's phase, and S(j + QST) is issued only after
+// that load, so no phase collects arrivals of two steps.
 enum {
   B_KV = 0,
-  B_S_FULL = 1,     // MMA -> compute warps: S^T in X
-  B_P_FULL = 2,     // compute warps -> MMA: P^T (bf16) in X, S^T read
-  B_DS_HALF = 3,    // compute warps -> MMA: the first 32 queries of each half of dS^T in TMEM
-  B_DP_FULL = 4,    // MMA -> compute warps: dP^T in Y
-  B_DS_FULL = 5,    // compute warps -> MMA: dS^T in TMEM and shared memory, dP^T read
-  B_DQ_FULL = 6,    // MMA -> drain: dQ (d = 64, in Z) or dQ^T (d = 128, in Y)
-  B_DQ_FREE = 7,    // drain -> MMA: dQ read, its region may be overwritten
-  B_MMA_DONE = 8,   // MMA -> epilogue and the MMA warp's drain: every MMA finished
-  B_Q_FULL = 9,     // [QST] Q tile + LSE2, D of a step
-  B_Q_EMPTY = 12,   // [QST]
-  B_O_FULL = 15,    // [OST] dO tile
-  B_O_EMPTY = 17,   // [OST]
-  B_COUNT = 19,
+  B_P_FULL = 1,     // compute warps -> MMA: P^T (bf16) in X, S^T read
+  B_DS_HALF = 2,    // compute warps -> MMA: the first 32 queries of each half of dS^T in TMEM
+  B_DP_FULL = 3,    // MMA -> compute warps: dP^T in Y
+  B_DS_FULL = 4,    // compute warps -> MMA: dS^T in TMEM and shared memory, dP^T read
+  B_DQ_FULL = 5,    // MMA -> drain: dQ (d = 64, in Z) or dQ^T (d = 128, in Y)
+  B_DQ_FREE = 6,    // drain -> MMA: dQ read, its region may be overwritten
+  B_MMA_DONE = 7,   // MMA -> epilogue and the MMA warp's drain: every MMA finished
+  B_S_FULL = 8,     // [QST] MMA + loader -> compute warps: S^T(i) in X, LSE2 and D of step i
+  B_Q_FULL = 11,    // [QST] Q tile of a step (TMA)
+  B_Q_EMPTY = 14,   // [QST] Q tile, LSE2 and D of a step no longer read
+  B_O_FULL = 17,    // [OST] dO tile
+  B_O_EMPTY = 19,   // [OST]
+  B_COUNT = 21,
 };
 static_assert(Bwd<128>::QST <= 3 && Bwd<64>::QST <= 3 && Bwd<64>::OST <= 2, "barrier slots");
 
@@ -262,7 +270,6 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
   // before the CTA-wide sync, so their latency overlaps the TMEM allocation.
   if (warp == 13 && lane == 0) {
     mbar_init(bar(B_KV), 1);
-    mbar_init(bar(B_S_FULL), 1);
     mbar_init(bar(B_P_FULL), 256);
     mbar_init(bar(B_DP_FULL), 1);
     mbar_init(bar(B_DS_HALF), 256);
@@ -271,7 +278,8 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
     mbar_init(bar(B_DQ_FREE), 128);
     mbar_init(bar(B_MMA_DONE), 1);
     for (int s = 0; s < QST; ++s) {
-      mbar_init(bar(B_Q_FULL + s), 1 + 32);
+      mbar_init(bar(B_S_FULL + s), 1 + 32);
+      mbar_init(bar(B_Q_FULL + s), 1);
       mbar_init(bar(B_Q_EMPTY + s), 1 + 256);
     }
     for (int s = 0; s < OST; ++s) {
@@ -335,7 +343,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
             stat[lane + 32 * j] = l[j];
             stat[BQ + lane + 32 * j] = dl[j];
           }
-          mbar_arrive(bar(B_Q_FULL + st));
+          mbar_arrive(bar(B_S_FULL + st));
         }
         {
           const int so = it % OST, use = it / OST;
@@ -416,7 +424,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
       if (ok) {
         tc_fence_after();
         mma_xyT(C::TM_X, sK, sQ(0));
-        mma_commit_w(bar(B_S_FULL));
+        mma_commit_w(bar(B_S_FULL + 0));
       }
       for (int it = 0; ok && it < n_it; ++it) {
         const bool next = it + 1 < n_it;
@@ -437,7 +445,7 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
           if (!(ok = wait_all(B_Q_FULL + (it + 1) % QST, (it + 1) / QST, 0x11))) break;
           tc_fence_after();
           mma_xyT(C::TM_X, sK, sQ(it + 1));
-          mma_commit_w(bar(B_S_FULL));
+          mma_commit_w(bar(B_S_FULL + (it + 1) % QST));
         }
         // dK(i) over the queries of the compute warps' first pass while they do
         // the second, then the rest of dK(i) and dQ(i) once dS^T(i) is complete
@@ -570,7 +578,6 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
     auto form_p = [&](int it) {
       const int st = it % QST;
       const int q0 = (i_start + it) * BQ;
-      mbar_wait(bar(B_Q_FULL + st), (it / QST) & 1, wctx, ERR_SITE_BWD | 0x21);
       const float4* nlse2 =
           reinterpret_cast<const float4*>(smem + C::OFF_STAT + st * 2 * BQ * 4) + 16 * w;
       // key kr sees query q iff kr < N and (not causal or kr <= q); queries
@@ -581,7 +588,8 @@ __global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
       int lo = 0;
       if (kr >= N) lo = 64;
       else if (p.causal) lo = min(max(kr - qh, 0), 64);
-      mbar_wait(bar(B_S_FULL), it & 1, wctx, ERR_SITE_BWD | 0x22);
+      // S^T(it) in X and this step's LSE2 in shared memory
+      mbar_wait(bar(B_S_FULL + st), (it / QST) & 1, wctx, ERR_SITE_BWD | 0x22);
       tc_fence_after();
       uint32_t u[2][32];
       tmem_ld32(tX, u[0]);

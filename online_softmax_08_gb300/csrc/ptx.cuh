@@ -61,6 +61,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Two or three phase tests issued back to back, so their latencies overlap; true
+// when every one of the phases has completed.
+__device__ __forceinline__ bool mbar_try_wait2(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 a, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 b, [%3], %4;\n\t"
+      "and.pred a, a, b;\n\t"
+      "selp.u32 %0, 1, 0, a;\n\t}"
+      : "=r"(ok)
+      : "r"(b0), "r"(p0), "r"(b1), "r"(p1)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_try_wait3(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1,
+                                               uint32_t b2, uint32_t p2) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred a, b, c;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 a, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 b, [%3], %4;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 c, [%5], %6;\n\t"
+      "and.pred a, a, b;\n\t"
+      "and.pred a, a, c;\n\t"
+      "selp.u32 %0, 1, 0, a;\n\t}"
+      : "=r"(ok)
+      : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+      : "memory");
+  return ok != 0;
+}
+
 // Per-CTA failure state: the abort flag lives in shared memory, the error
 // word in global memory (first failure wins).
 struct WaitCtx {

@@ -180,6 +180,30 @@ def test_null_workspace_uses_stream_ordered_scratch():
         _check(_f64(got), r, name)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N,reps", [(2, 3, 1100, 20), (4, 16, 2048, 10)])
+def test_repeated_backward_calls(B, H, N, reps, d, causal):
+    """Repeated calls on the same inputs: a missed barrier or a stage reused too
+    early would show up as calls that disagree.  dK and dV accumulate in TMEM in a
+    fixed order, so every call gives them bit for bit; dQ's fp32 partials are added
+    in whatever order the CTAs reach the accumulator, so calls may differ by one
+    bf16 step (2^-7 relative) plus the partial sums' fp32 rounding."""
+    q, k, v, do = make_inputs(B, H, N, d, seed=940 + d + int(causal), with_do=True)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    scale = default_scale(d)
+    o, lse = fattn.forward(qd, kd, vd, scale, causal)
+    dq0, dk0, dv0 = fattn.backward(qd, kd, vd, o, lse, dod, scale, causal)
+    for _ in range(reps):
+        dq, dk, dv = fattn.backward(qd, kd, vd, o, lse, dod, scale, causal)
+        assert torch.equal(dk, dk0) and torch.equal(dv, dv0)
+        a, b = dq.float(), dq0.float()
+        assert bool(((a - b).abs() <= torch.maximum(a.abs(), b.abs()) * 2.0**-7 + 1e-5).all())
+    torch.cuda.synchronize()
+    assert fattn.fattn_device_error() == 0
+
+
 def test_backward_argument_checks():
     dev = torch.device("cuda:0")
     x = torch.zeros(1, 1, 128, 128, dtype=torch.bfloat16, device=dev)

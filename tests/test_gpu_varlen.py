@@ -63,6 +63,31 @@ def test_varlen_forward_and_backward_match_oracle(lengths, H, d, causal):
         _close(_f64(got), want)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_repeated_varlen_backward_calls(d):
+    """Repeated varlen backward calls agree: dK and dV bit for bit, dQ within one bf16
+    step.  Lengths off multiples of 32 and 128 leave the dQ boxes of a sequence's
+    last query block reaching into the next sequence's rows (adding exact zeros)
+    while that sequence's own CTAs add into them."""
+    lengths = [777, 95, 1000, 33, 513, 260]
+    q, k, v, do, cu = make_varlen_inputs(lengths, 3, d, seed=1944 + d, with_do=True)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod, cud = (x.to(dev) for x in (q, k, v, do, cu))
+    scale = default_scale(d)
+    for causal in (False, True):
+        o, lse = fattn.forward_varlen(qd, kd, vd, cud, max(lengths), scale, causal)
+        dq0, dk0, dv0 = fattn.backward_varlen(qd, kd, vd, o, lse, dod, cud, max(lengths), scale,
+                                              causal)
+        for _ in range(15):
+            dq, dk, dv = fattn.backward_varlen(qd, kd, vd, o, lse, dod, cud, max(lengths), scale,
+                                               causal)
+            assert torch.equal(dk, dk0) and torch.equal(dv, dv0)
+            a, b = dq.float(), dq0.float()
+            assert bool(((a - b).abs() <= torch.maximum(a.abs(), b.abs()) * 2.0**-7 + 1e-5).all())
+    torch.cuda.synchronize()
+    assert fattn.fattn_device_error() == 0
+
+
 def test_varlen_d64_grid_of_two_subtile_ctas():
     """The d = 64 varlen forward on a grid large enough (from the device's SM
     count) for two 128-row subtiles per CTA, forward and backward against the

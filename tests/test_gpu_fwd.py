@@ -173,9 +173,10 @@ def test_b4h16_n2048_d64_all_heads(causal):
 def test_d64_grid_of_two_subtile_ctas(causal):
     """At d = 64 the launcher gives each CTA one 128-row subtile (two CTAs per
     SM) while the two-subtile grid would be at most six waves, and two subtiles
-    per CTA beyond that.  C2 and the small cases take the first form; this
-    shape, sized from the device's SM count, takes the second.  Four heads are
-    compared element by element, and the tile counts of all of them."""
+    per CTA beyond that.  The B 4, H 16, N 2048 workload and the small cases take
+    the first form; this shape, sized from the device's SM count, takes the
+    second.  Four heads are compared element by element, and the tile counts of
+    all of them."""
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
     N, d = 2048, 64
     H = 16
